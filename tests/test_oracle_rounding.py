@@ -1,0 +1,102 @@
+"""Pins for the oracle's P rounding ("在 agent 时代如何快速验证 kernel 对精度的影响",
+section "注意力权重")."""
+
+import itertools
+
+import numpy as np
+import torch
+
+from conftest import read_golden
+from oracle import rounding as R
+
+
+def e4m3_values():
+    """All non-negative finite OCP E4M3 values, decoded from their bit fields
+    (bias 7; exponent field 0 = subnormal; S.1111.111 is NaN)."""
+    vals = []
+    for e, m in itertools.product(range(16), range(8)):
+        if e == 15 and m == 7:
+            continue
+        vals.append((m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return np.array(sorted(vals))
+
+
+def brute_nearest_even(v, grid, mant_of):
+    """Nearest grid value; ties go to the value with an even mantissa."""
+    d = np.abs(grid - v)
+    best = np.flatnonzero(d == d.min())
+    if len(best) == 1:
+        return grid[best[0]]
+    return [grid[i] for i in best if mant_of(grid[i]) % 2 == 0][0]
+
+
+def test_e4m3_grid_facts():
+    grid = e4m3_values()
+    assert grid.max() == 448.0
+    assert grid[1] == 2.0 ** -9
+    assert len(grid) == 127
+
+
+def test_e4m3_page_thresholds():
+    g = read_golden("e4m3_thresholds.txt")
+    assert R.e4m3(np.float32(1.0)) == 1.0
+    assert R.e4m3(np.float32(448.0)) == float(g["e4m3_max"])
+    smallest = R.e4m3(np.float32(0.002))
+    assert smallest == 2.0 ** -9                       # "about 0.002"
+    assert abs(smallest - float(g["smallest_positive_approx"])) < 1e-4
+    assert R.e4m3(np.float32(2.0 ** -10)) == 0.0       # half of it: tie -> even (0)
+    assert R.e4m3(np.float32(0.00098)) == 2.0 ** -9    # just above half
+    assert R.e4m3(np.float32(0.0009)) == 0.0           # below "about 0.001"
+    assert abs(2.0 ** -10 - float(g["flush_below_approx"])) < 1e-4
+    # x448 variant: the smallest p that survives is just above 2^-10 / 448
+    thr = 2.0 ** -10 / 448
+    assert thr < float(g["x448_threshold_max"])        # "a few per million"
+    assert R.round_p(np.float32(thr * 1.01), 3) > 0
+    assert R.round_p(np.float32(thr * 0.99), 3) == 0
+
+
+def test_e4m3_brute_force_nearest():
+    grid = e4m3_values()
+
+    def mant(v):
+        i = int(np.flatnonzero(grid == v)[0])
+        return i  # grid index parity equals mantissa-field parity
+    rng = np.random.default_rng(3)
+    vs = np.concatenate([rng.uniform(0, 448, 3000), rng.uniform(0, 0.02, 2000),
+                         grid, (grid[1:] + grid[:-1]) / 2]).astype(np.float32)
+    got = R.e4m3(vs)
+    for v, g in zip(vs, got):
+        assert g == brute_nearest_even(float(v), grid, mant), v
+
+
+def test_e4m3_matches_torch_float8():
+    rng = np.random.default_rng(4)
+    vs = np.concatenate([rng.uniform(0, 448, 20000), rng.uniform(0, 0.05, 20000),
+                         np.exp(rng.uniform(-20, 0, 20000))]).astype(np.float32)
+    ref = torch.from_numpy(vs).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(R.e4m3(vs), ref)
+
+
+def test_bf16_matches_torch_and_bit_rounding():
+    rng = np.random.default_rng(5)
+    vs = np.concatenate([rng.uniform(0, 1, 20000), np.exp(rng.uniform(-100, 0, 20000)),
+                         np.array([1e-40, 3e-39, 1.0, 0.0])]).astype(np.float32)
+    ref = torch.from_numpy(vs).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(R.bf16(vs), ref)
+    # round-to-nearest-even on the bit pattern
+    u = vs.view(np.uint32).astype(np.uint64)
+    rne = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    assert np.array_equal(R.bf16(vs), rne.view(np.float32).astype(np.float64))
+
+
+def test_round_p_modes():
+    p = np.float32([1.0, 0.5, 0.3, 1e-3, 1e-7, 0.0])
+    assert np.array_equal(R.round_p(p, 0), p.astype(np.float64))
+    for mode in range(4):
+        assert R.round_p(np.float32(1.0), mode) == 1.0   # p = 1 is kept by all
+        assert R.round_p(np.float32(0.0), mode) == 0.0
+    # x448: scale, round, unscale
+    x = np.float32(0.3)
+    assert R.round_p(x, 3) == R.e4m3(np.float32(x * np.float32(448))) / 448
+    # exact-mode variant divides in float32
+    assert R.round_p_f32(x, 3) == np.float32(np.float32(R.e4m3(x * np.float32(448))) / np.float32(448))
