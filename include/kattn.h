@@ -1,0 +1,193 @@
+/*
+ * kattn.h -- C ABI for decode attention over an int8-quantized KV cache
+ * on NVIDIA GB300 (sm_103a).
+ *
+ * The operation (sources cited by page title and section):
+ *
+ *   "Kestrel_VLLM - 18 · 投机解码位级对拍收口" (wsisp.com)
+ *     §3.3  decode attention with an int8 query quantized per head, int32
+ *           QK dot products against int8 K rows, online softmax over the
+ *           tokens, sequential P.V; and the table-driven expf used by the
+ *           bit-exact variant.
+ *     §二   speculative batch verify: draft column j of an M-column batch
+ *           must reproduce, byte for byte, an M=1 decode that saw the same
+ *           tokens.
+ *     §四   the per-layer cache fields: int8 K/V rows with one float scale
+ *           per row (_k _ks _v _vs).
+ *   "在 agent 时代如何快速验证 kernel 对精度的影响" (susun-blog.com)
+ *     section "注意力权重：直接转 fp8 随上下文变差，先放大就和 bf16 差不多":
+ *           blockwise online softmax where only the P that multiplies V is
+ *           rounded (f32 / bf16 / fp8 e4m3 / x448 then e4m3), the row sum
+ *           uses the unrounded P, and the output is divided by it at the end.
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers owned by the caller; the
+ *     library never frees or retains them.  No entry point allocates
+ *     device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it; arguments are
+ *     validated on the host before anything is enqueued, and an invalid
+ *     call enqueues nothing.
+ *   - The return value is a kattn_status (0 = success, < 0 = error).
+ *     KATTN_ERR_CUDA means a CUDA runtime call (launch or copy) failed;
+ *     the CUDA error is left for the caller to query.
+ *   - Layouts are dense row-major with the sizes given.  head_dim d must
+ *     be 128.  Pointers to int8 or float arrays must be 16-byte aligned.
+ *   - Values must be finite; behaviour for NaN or Inf inputs is undefined
+ *     (no fault, unspecified output).
+ */
+#ifndef KATTN_H
+#define KATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status -- */
+enum kattn_status {
+  KATTN_OK = 0,
+  KATTN_ERR_INVALID_ARG = -1, /* null pointer, negative or inconsistent size */
+  KATTN_ERR_UNSUPPORTED = -2, /* d != 128, M > KATTN_MAX_M, g*M > KATTN_MAX_ROWS */
+  KATTN_ERR_MISALIGNED = -3,  /* a pointer or stride is not 16-byte aligned */
+  KATTN_ERR_WORKSPACE = -4,   /* workspace missing, too small or unaligned */
+  KATTN_ERR_CUDA = -5         /* a CUDA runtime call failed */
+};
+
+/* P rounding applied to the weights that multiply V (the row sum always uses
+ * the unrounded weight): see the susun-blog page, section "注意力权重". */
+enum kattn_p_mode {
+  KATTN_P_F32 = 0,      /* keep float32 */
+  KATTN_P_BF16 = 1,     /* round to bfloat16, nearest-even */
+  KATTN_P_E4M3 = 2,     /* round to fp8 e4m3 (OCP), nearest-even, saturating */
+  KATTN_P_E4M3_X448 = 3 /* e4m3(p * 448) / 448 */
+};
+
+#define KATTN_HEAD_DIM 128 /* the only supported head_dim */
+#define KATTN_MAX_M 8      /* draft columns per sequence */
+#define KATTN_MAX_ROWS 64  /* g * M query rows per (sequence, kv head) */
+
+/* Device error bits reported by kattn_get_device_status. */
+#define KATTN_DEVERR_BAD_SEQUENCE 0x1u /* row_start / ctx_len out of range */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* kattn_status_string(int status);
+
+/* Fixed tiling of the fast decode path.
+ * *split_C: keys per split.  The keys of every sequence are cut into splits
+ *   at absolute positions [s*C, (s+1)*C); each split is reduced on its own
+ *   and the splits are merged in split order.  C is a compile-time constant,
+ *   so the result for a query row depends only on its own keys -- never on
+ *   the batch size, M, or other sequences (batch invariance, "Kestrel_VLLM -
+ *   18" §二).
+ * *round_block_Bk: keys per online-softmax block inside a split; the running
+ *   max that a rounded P is taken relative to is updated once per block.
+ * Either pointer may be NULL.  Never fails. */
+int kattn_get_tiling(int* split_C, int* round_block_Bk);
+
+/* Bytes of workspace kattn_decode needs for these sizes (fast mode; exact
+ * mode needs none).  max_ctx is the host-side upper bound on ctx_len.
+ * Returns 0 for invalid sizes.  Before the FIRST call with a workspace, the
+ * caller must zero it (e.g. cudaMemsetAsync); every completed kattn_decode
+ * leaves its counters at zero again, so one workspace may be reused by any
+ * number of calls that are ordered on the GPU.  Calls that share a workspace
+ * and overlap on the GPU race and give undefined results. */
+size_t kattn_decode_workspace_size(int B, int M, int Hq, int max_ctx);
+
+/* Quantize K or V rows into the int8 cache ("Kestrel_VLLM - 18" §四 fields
+ * _k/_ks, _v/_vs).  For each row r < n_rows and kv head h < n_kv:
+ *   scale = f32(max_i |x[r][h][i]|) / 127                (IEEE division)
+ *   q[i]  = clamp(rint_half_even(x[r][h][i] / scale), -127, 127); scale 0 -> 0
+ *   out_q[(h*cap_rows + dst_row0 + r)*d + i] = q[i]
+ *   out_scale[h*cap_rows + dst_row0 + r]     = scale
+ * x:       float32, row r of head h at x + r*row_stride_elems + h*d
+ *          (row_stride_elems >= n_kv*d, a multiple of 4).
+ * out_q:   int8 cache [n_kv][cap_rows][d];  out_scale: float32 [n_kv][cap_rows].
+ * Requires 0 <= dst_row0 and dst_row0 + n_rows <= cap_rows.  n_rows == 0 is
+ * a no-op.  Bitwise deterministic. */
+int kattn_quantize_kv(const float* x, int n_rows, int n_kv, int d,
+                      int64_t row_stride_elems, int8_t* out_q, float* out_scale,
+                      int64_t dst_row0, int cap_rows, void* stream);
+
+/* Append form of kattn_quantize_kv: row r of x is quantized into cache row
+ * dst_rows[r] of every kv head (one launch for rows scattered over many
+ * sequences, e.g. the draft tokens of a decode step).
+ * dst_rows: int64 [n_rows] on the device.  Because it lives on the device it
+ * is checked there: a row whose index is outside [0, cap_rows) is skipped and
+ * nothing is written for it.  Two rows with the same index race.  Other
+ * arguments, the formula, alignment and errors as in kattn_quantize_kv. */
+int kattn_quantize_kv_rows(const float* x, int n_rows, int n_kv, int d,
+                           int64_t row_stride_elems, const int64_t* dst_rows, int8_t* out_q,
+                           float* out_scale, int cap_rows, void* stream);
+
+/* Decode attention ("Kestrel_VLLM - 18" §3.3; the susun-blog page, section
+ * "注意力权重").  For sequence b < B, draft column j < M, query head h < Hq
+ * (kv head kh = h / g, g = Hq / Hkv):
+ *   (q8, qs)  = absmax/127 int8 quantization of q[b][j][h][:]
+ *   L         = ctx_len[b] + j      (column j sees the context and drafts 0..j)
+ *   keys t < L are cache rows row_start[b] + t of head kh
+ *   S_t       = sum_i q8[i] * k[kh][row_start[b]+t][i]          (exact int32)
+ *   s_t       = ((float)S_t * (qs * k_scale[kh][row])) * sm_scale
+ *   out[b][j][h][:] = sum_t softmax(s)_t * (v_scale[kh][row] * v[kh][row][:])
+ *   with P rounded per p_mode before it multiplies V.
+ * q:         float32 [B][M][Hq][d].
+ * k, v:      int8 [Hkv][cap_rows][d];  k_scale, v_scale: float32 [Hkv][cap_rows].
+ * row_start: int64 [B] (device); ctx_len: int32 [B] (device), each >= 1 and
+ *            <= max_ctx, with row_start[b] + ctx_len[b] + M - 1 <= cap_rows.
+ *            These two arrays live on the device, so they are checked on the
+ *            device: a sequence that breaks the rule gets NaN outputs and sets
+ *            KATTN_DEVERR_BAD_SEQUENCE in the workspace (exact mode: no flag,
+ *            NaN outputs only); no memory outside the arrays is touched.
+ * max_ctx:   host-side upper bound on ctx_len (sizes the grid).
+ * sm_scale:  0 selects RN_f32(1/sqrt(d)).
+ * p_mode:    a kattn_p_mode.
+ * exact_mode = 0 (fast): split-KV over splits of C keys, merged in a fixed
+ *   order; float32 throughout; deterministic run to run, and the bytes of
+ *   out[b][j][h] depend only on that row's own keys, so column j equals an
+ *   M=1 call with ctx_len + j, in any batch.  Needs a workspace of
+ *   kattn_decode_workspace_size(B, M, Hq, max_ctx) bytes, 256-byte aligned.
+ * exact_mode = 1: one token at a time in token order; every float32
+ *   operation rounded separately (no contraction); exp by the table-driven
+ *   method of "Kestrel_VLLM - 18" §3.3 (64-entry 2^(j/64) table, 3-term
+ *   polynomial, double fused multiply-adds).  Bit-exact against the CPU
+ *   oracle's sequential emulation.  workspace may be NULL.
+ * out:       float32 [B][M][Hq][d]. */
+int kattn_decode(const float* q, const int8_t* k, const float* k_scale,
+                 const int8_t* v, const float* v_scale, const int64_t* row_start,
+                 const int32_t* ctx_len, int B, int M, int Hq, int Hkv, int d,
+                 int cap_rows, int max_ctx, float sm_scale, int p_mode,
+                 int exact_mode, float* out, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* Integer QK scores of the decode path, for parity checks ("Kestrel_VLLM -
+ * 18" §3.3: int8 query quantization + int32 QK dot product).
+ * scores: int32 [B][M][Hq][max_ctx + M - 1]; entry t of row (b, j, h) is
+ *   written for t < ctx_len[b] + j and left untouched otherwise.
+ * q_i8:   optional int8 [B][M][Hq][d] quantized queries (NULL to skip).
+ * q_scale: optional float32 [B][M][Hq] query scales (NULL to skip).
+ * Other arguments as in kattn_decode.  Sequences that break the row_start /
+ * ctx_len rule are skipped (their scores are left untouched). */
+int kattn_qk_scores_debug(const float* q, const int8_t* k, const float* k_scale,
+                          const int64_t* row_start, const int32_t* ctx_len, int B,
+                          int M, int Hq, int Hkv, int d, int cap_rows, int max_ctx,
+                          int32_t* scores, int8_t* q_i8, float* q_scale, void* stream);
+
+/* The constants exact mode uses for its table-driven exp ("Kestrel_VLLM - 18"
+ * §3.3), as the library derived them on the host: out68[0..3] = K = RN(64/ln2),
+ * C2 = RN(ln2/64), C0 = RN(1/6), C1 = 1/2; out68[4 + j] = RN(2^(j/64)) for
+ * j < 64.  Host only; for parity checks.  Returns KATTN_ERR_INVALID_ARG if
+ * out68 is NULL. */
+int kattn_expf_constants(double* out68);
+
+/* Read (and clear) the device error word of a decode workspace.  Copies 4
+ * bytes to the host and waits for `stream`.  *device_err receives the
+ * KATTN_DEVERR_* bits set by calls since the last read. */
+int kattn_get_device_status(void* workspace, size_t workspace_bytes,
+                            int* device_err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KATTN_H */

@@ -1,0 +1,19 @@
+"""int8-KV decode attention for NVIDIA GB300 (sm_103a).
+
+The compute lives in libkattn.so (hand-written CUDA kernels behind the C ABI
+in include/kattn.h); this package is a thin torch-facing binding.
+"""
+
+from .api import (  # noqa: F401
+    P_MODES,
+    alloc_workspace,
+    decode,
+    decode_workspace_size,
+    expf_constants,
+    get_device_status,
+    get_tiling,
+    qk_scores_debug,
+    quantize_kv,
+    quantize_kv_rows,
+)
+from ._lib import KattnError, LIB_PATH, load  # noqa: F401

@@ -1,0 +1,179 @@
+"""Python binding over the kattn C ABI (argument marshalling only).
+
+Every function takes torch CUDA tensors, checks dtypes/shapes/contiguity,
+and passes raw device pointers plus torch's current CUDA stream to the
+library.  All computation happens in the library's CUDA kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+P_MODES = {"f32": 0, "bf16": 1, "e4m3": 2, "e4m3x448": 3}
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _need(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+def get_tiling() -> tuple:
+    lib = _lib.load()
+    c, bk = ctypes.c_int(), ctypes.c_int()
+    lib.kattn_get_tiling(ctypes.byref(c), ctypes.byref(bk))
+    return c.value, bk.value
+
+
+def expf_constants() -> list:
+    """The library's exact-mode exp constants: [K, C2, C0, C1, T[0..63]]."""
+    lib = _lib.load()
+    buf = (ctypes.c_double * 68)()
+    _lib.check("kattn_expf_constants", lib.kattn_expf_constants(buf))
+    return list(buf)
+
+
+def decode_workspace_size(B: int, M: int, Hq: int, max_ctx: int) -> int:
+    return int(_lib.load().kattn_decode_workspace_size(B, M, Hq, max_ctx))
+
+
+def alloc_workspace(B: int, M: int, Hq: int, max_ctx: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for kattn_decode (allocated by torch, not the library)."""
+    n = decode_workspace_size(B, M, Hq, max_ctx)
+    if n == 0:
+        raise ValueError("invalid sizes for a decode workspace")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def quantize_kv(x: torch.Tensor, out_q: torch.Tensor, out_scale: torch.Tensor,
+                dst_row0: int = 0) -> None:
+    """x [n_rows][Hkv][d] float32 -> out_q [Hkv][cap][d] int8, out_scale [Hkv][cap]."""
+    _need(x, torch.float32, "x", 3)
+    _need(out_q, torch.int8, "out_q", 3)
+    _need(out_scale, torch.float32, "out_scale", 2)
+    n_rows, n_kv, d = x.shape
+    cap = out_q.shape[1]
+    if out_q.shape[0] != n_kv or out_q.shape[2] != d or tuple(out_scale.shape) != (n_kv, cap):
+        raise ValueError("cache shapes do not match x")
+    lib = _lib.load()
+    _lib.check("kattn_quantize_kv", lib.kattn_quantize_kv(
+        _ptr(x), n_rows, n_kv, d, n_kv * d, _ptr(out_q), _ptr(out_scale), dst_row0, cap,
+        _stream(x.device)))
+
+
+def quantize_kv_rows(x: torch.Tensor, dst_rows: torch.Tensor, out_q: torch.Tensor,
+                     out_scale: torch.Tensor) -> None:
+    """Append form: row r of x [n_rows][Hkv][d] goes to cache row dst_rows[r]."""
+    _need(x, torch.float32, "x", 3)
+    _need(dst_rows, torch.int64, "dst_rows", 1)
+    _need(out_q, torch.int8, "out_q", 3)
+    _need(out_scale, torch.float32, "out_scale", 2)
+    n_rows, n_kv, d = x.shape
+    cap = out_q.shape[1]
+    if dst_rows.numel() != n_rows:
+        raise ValueError("dst_rows must have one entry per row of x")
+    if out_q.shape[0] != n_kv or out_q.shape[2] != d or tuple(out_scale.shape) != (n_kv, cap):
+        raise ValueError("cache shapes do not match x")
+    lib = _lib.load()
+    _lib.check("kattn_quantize_kv_rows", lib.kattn_quantize_kv_rows(
+        _ptr(x), n_rows, n_kv, d, n_kv * d, _ptr(dst_rows), _ptr(out_q), _ptr(out_scale), cap,
+        _stream(x.device)))
+
+
+def decode(q, k, k_scale, v, v_scale, row_start, ctx_len, max_ctx: int, *,
+           out=None, p_mode=0, exact_mode=False, sm_scale: float = 0.0, workspace=None):
+    """Decode attention; returns out [B][M][Hq][d] float32.
+
+    q [B][M][Hq][d] f32; k, v [Hkv][cap][d] int8; k_scale, v_scale [Hkv][cap]
+    f32; row_start [B] int64; ctx_len [B] int32 (all on the same CUDA device).
+    workspace: a zeroed uint8 tensor of decode_workspace_size(...) bytes
+    (fast mode); allocated here with torch if None.
+    """
+    _need(q, torch.float32, "q", 4)
+    _need(k, torch.int8, "k", 3)
+    _need(v, torch.int8, "v", 3)
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(v_scale, torch.float32, "v_scale", 2)
+    _need(row_start, torch.int64, "row_start", 1)
+    _need(ctx_len, torch.int32, "ctx_len", 1)
+    B, M, Hq, d = q.shape
+    Hkv, cap, _ = k.shape
+    if tuple(v.shape) != tuple(k.shape) or tuple(k_scale.shape) != (Hkv, cap) \
+            or tuple(v_scale.shape) != (Hkv, cap):
+        raise ValueError("k/v/scales shapes disagree")
+    if row_start.numel() != B or ctx_len.numel() != B:
+        raise ValueError("row_start / ctx_len must have B entries")
+    mode = P_MODES.get(p_mode, p_mode) if isinstance(p_mode, str) else int(p_mode)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, torch.float32, "out", 4)
+    ws_bytes = 0
+    if not exact_mode:
+        if workspace is None:
+            workspace = alloc_workspace(B, M, Hq, max_ctx, q.device)
+        _need(workspace, torch.uint8, "workspace", 1)
+        ws_bytes = workspace.numel()
+    lib = _lib.load()
+    _lib.check("kattn_decode", lib.kattn_decode(
+        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(v), _ptr(v_scale), _ptr(row_start), _ptr(ctx_len),
+        B, M, Hq, Hkv, d, cap, int(max_ctx), float(sm_scale), mode, 1 if exact_mode else 0,
+        _ptr(out), _ptr(workspace) if not exact_mode else 0, ws_bytes, _stream(q.device)))
+    return out
+
+
+def qk_scores_debug(q, k, k_scale, row_start, ctx_len, max_ctx: int, *, scores=None,
+                    want_q=False):
+    """Integer QK scores [B][M][Hq][max_ctx + M - 1] (int32); entries t >= L_j
+    keep their prior contents (filled with INT32_MIN when allocated here).
+    With want_q, also returns (q_i8, q_scale)."""
+    _need(q, torch.float32, "q", 4)
+    _need(k, torch.int8, "k", 3)
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(row_start, torch.int64, "row_start", 1)
+    _need(ctx_len, torch.int32, "ctx_len", 1)
+    B, M, Hq, d = q.shape
+    Hkv, cap, _ = k.shape
+    width = int(max_ctx) + M - 1
+    if scores is None:
+        scores = torch.full((B, M, Hq, width), -2 ** 31, dtype=torch.int32, device=q.device)
+    else:
+        _need(scores, torch.int32, "scores", 4)
+    q_i8 = q_scale = None
+    if want_q:
+        q_i8 = torch.zeros((B, M, Hq, d), dtype=torch.int8, device=q.device)
+        q_scale = torch.zeros((B, M, Hq), dtype=torch.float32, device=q.device)
+    lib = _lib.load()
+    _lib.check("kattn_qk_scores_debug", lib.kattn_qk_scores_debug(
+        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(row_start), _ptr(ctx_len), B, M, Hq, Hkv, d, cap,
+        int(max_ctx), _ptr(scores), _ptr(q_i8), _ptr(q_scale), _stream(q.device)))
+    return (scores, q_i8, q_scale) if want_q else scores
+
+
+def get_device_status(workspace: torch.Tensor) -> int:
+    """Read and clear the device error bits of a decode workspace."""
+    _need(workspace, torch.uint8, "workspace", 1)
+    lib = _lib.load()
+    err = ctypes.c_int(0)
+    _lib.check("kattn_get_device_status", lib.kattn_get_device_status(
+        _ptr(workspace), workspace.numel(), ctypes.byref(err), _stream(workspace.device)))
+    return err.value

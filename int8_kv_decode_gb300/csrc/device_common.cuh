@@ -1,0 +1,100 @@
+// Device helpers shared by the kattn kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "kattn_internal.cuh"
+
+namespace kattn {
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Butterfly sum: every lane ends with the same value, summed in a fixed order.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Per-row int8 quantization ("Kestrel_VLLM - 18" §3.3 int8 query; cache
+// fields §四): scale = f32(absmax)/127, q = clamp(rint_even(x/scale), +-127),
+// zero row -> 0.  Both divisions are IEEE float32.
+__device__ __forceinline__ float quant_scale(float amax) {
+  return __fdiv_rn(amax, 127.0f);
+}
+
+__device__ __forceinline__ int quant_one(float x, float scale) {
+  if (scale == 0.0f) return 0;
+  int q = __float2int_rn(__fdiv_rn(x, scale));
+  return max(-127, min(127, q));
+}
+
+__device__ __forceinline__ uint32_t pack_i8x4(int a, int b, int c, int d) {
+  return (uint32_t)(a & 0xff) | ((uint32_t)(b & 0xff) << 8) |
+         ((uint32_t)(c & 0xff) << 16) | ((uint32_t)(d & 0xff) << 24);
+}
+
+// One warp quantizes one 128-element float row: lane l owns elements
+// 4l..4l+3.  Returns the packed int8x4 word for the lane and the scale.
+__device__ __forceinline__ uint32_t warp_quantize_row(const float* __restrict__ row,
+                                                      float* scale_out) {
+  const int lane = threadIdx.x & 31;
+  float4 x = reinterpret_cast<const float4*>(row)[lane];
+  float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+  amax = warp_max(amax);
+  float s = quant_scale(amax);
+  *scale_out = s;
+  return pack_i8x4(quant_one(x.x, s), quant_one(x.y, s), quant_one(x.z, s),
+                   quant_one(x.w, s));
+}
+
+// Rounding of P before it multiplies V (susun-blog page, section "注意力权重").
+__device__ __forceinline__ float e4m3_round(float x) {
+  __nv_fp8_storage_t s = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+  __half_raw h = __nv_cvt_fp8_to_halfraw(s, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Row (b, column j) validity: the cache rows it reads must lie in the arrays.
+__device__ __forceinline__ bool sequence_ok(int64_t rs, int ctx, int M, int cap_rows,
+                                            int max_ctx) {
+  return ctx >= 1 && ctx <= max_ctx && rs >= 0 &&
+         rs + (int64_t)ctx + (int64_t)(M - 1) <= (int64_t)cap_rows;
+}
+
+// ------------------------------------------------------------ cp.async ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte copy global -> shared; src_bytes < 16 zero-fills the rest.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)),
+               "l"(src), "r"(src_bytes));
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(dst)),
+               "l"(src), "r"(src_bytes));
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+}  // namespace kattn

@@ -1,0 +1,199 @@
+// C ABI entry points (include/kattn.h): host-side validation and launches.
+#include <cmath>
+#include <cstring>
+
+#include "kattn_internal.cuh"
+
+using namespace kattn;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+float resolve_sm_scale(float sm_scale, int d) {
+  // RN_f32(1/sqrt(d)): sqrt and the division are correctly rounded in double,
+  // and for d = 128 the double is far from a float32 rounding tie.
+  return sm_scale != 0.0f ? sm_scale : (float)(1.0 / std::sqrt((double)d));
+}
+
+// Shared argument checks of kattn_decode and kattn_qk_scores_debug.
+int check_common(const float* q, const int8_t* k, const float* k_scale,
+                 const int64_t* row_start, const int32_t* ctx_len, int B, int M, int Hq,
+                 int Hkv, int d, int cap_rows, int max_ctx) {
+  if (B < 0 || M < 1 || Hq < 1 || Hkv < 1 || cap_rows < 1 || max_ctx < 1)
+    return KATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || B > 65535 || Hkv > 65535) return KATTN_ERR_INVALID_ARG;
+  if (d != KATTN_HEAD_DIM) return KATTN_ERR_UNSUPPORTED;
+  if (M > KATTN_MAX_M || (Hq / Hkv) * M > KATTN_MAX_ROWS) return KATTN_ERR_UNSUPPORTED;
+  if ((int64_t)max_ctx + M - 1 > (int64_t)INT32_MAX / 2) return KATTN_ERR_INVALID_ARG;
+  if (B == 0) return KATTN_OK;
+  if (!q || !k || !k_scale || !row_start || !ctx_len) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(k_scale, 4) || !aligned(row_start, 8) ||
+      !aligned(ctx_len, 4))
+    return KATTN_ERR_MISALIGNED;
+  return KATTN_OK;
+}
+
+DecodeParams make_params(const float* q, const int8_t* k, const float* k_scale,
+                         const int8_t* v, const float* v_scale, const int64_t* row_start,
+                         const int32_t* ctx_len, int B, int M, int Hq, int Hkv, int cap_rows,
+                         int max_ctx, float sm_scale, int p_mode, float* out) {
+  DecodeParams p{};
+  p.q = q;
+  p.k = k;
+  p.k_scale = k_scale;
+  p.v = v;
+  p.v_scale = v_scale;
+  p.row_start = row_start;
+  p.ctx_len = ctx_len;
+  p.out = out;
+  p.B = B;
+  p.M = M;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.g = Hq / Hkv;
+  p.R = p.g * M;
+  p.cap_rows = cap_rows;
+  p.max_ctx = max_ctx;
+  p.nsplit_max = nsplit_for(max_ctx + M - 1);
+  p.sm_scale = resolve_sm_scale(sm_scale, KATTN_HEAD_DIM);
+  p.p_mode = p_mode;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kattn_status_string(int status) {
+  switch (status) {
+    case KATTN_OK: return "KATTN_OK";
+    case KATTN_ERR_INVALID_ARG: return "KATTN_ERR_INVALID_ARG";
+    case KATTN_ERR_UNSUPPORTED: return "KATTN_ERR_UNSUPPORTED";
+    case KATTN_ERR_MISALIGNED: return "KATTN_ERR_MISALIGNED";
+    case KATTN_ERR_WORKSPACE: return "KATTN_ERR_WORKSPACE";
+    case KATTN_ERR_CUDA: return "KATTN_ERR_CUDA";
+    default: return "KATTN_UNKNOWN_STATUS";
+  }
+}
+
+int kattn_get_tiling(int* split_C, int* round_block_Bk) {
+  if (split_C) *split_C = kSplitC;
+  if (round_block_Bk) *round_block_Bk = kTileBk;
+  return KATTN_OK;
+}
+
+size_t kattn_decode_workspace_size(int B, int M, int Hq, int max_ctx) {
+  if (B < 1 || M < 1 || M > KATTN_MAX_M || Hq < 1 || max_ctx < 1) return 0;
+  return workspace_layout(B, M, Hq, max_ctx).total;
+}
+
+int kattn_expf_constants(double* out68) {
+  if (!out68) return KATTN_ERR_INVALID_ARG;
+  const ExpfConsts& c = expf_constants();
+  out68[0] = c.K;
+  out68[1] = c.C2;
+  out68[2] = c.C0;
+  out68[3] = c.C1;
+  for (int j = 0; j < 64; ++j) out68[4 + j] = c.T[j];
+  return KATTN_OK;
+}
+
+int kattn_quantize_kv(const float* x, int n_rows, int n_kv, int d, int64_t row_stride_elems,
+                      int8_t* out_q, float* out_scale, int64_t dst_row0, int cap_rows,
+                      void* stream) {
+  if (n_rows < 0 || n_kv < 1 || cap_rows < 1 || dst_row0 < 0) return KATTN_ERR_INVALID_ARG;
+  if (d != KATTN_HEAD_DIM) return KATTN_ERR_UNSUPPORTED;
+  if (dst_row0 + (int64_t)n_rows > (int64_t)cap_rows) return KATTN_ERR_INVALID_ARG;
+  if (row_stride_elems < (int64_t)n_kv * d) return KATTN_ERR_INVALID_ARG;
+  if (n_rows == 0) return KATTN_OK;
+  if (!x || !out_q || !out_scale) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || row_stride_elems % 4 != 0 || !aligned(out_q, 16) ||
+      !aligned(out_scale, 4))
+    return KATTN_ERR_MISALIGNED;
+  cudaError_t e = launch_quantize_kv(x, n_rows, n_kv, row_stride_elems, out_q, out_scale,
+                                     dst_row0, nullptr, cap_rows, as_stream(stream));
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+}
+
+int kattn_quantize_kv_rows(const float* x, int n_rows, int n_kv, int d,
+                           int64_t row_stride_elems, const int64_t* dst_rows, int8_t* out_q,
+                           float* out_scale, int cap_rows, void* stream) {
+  if (n_rows < 0 || n_kv < 1 || cap_rows < 1) return KATTN_ERR_INVALID_ARG;
+  if (d != KATTN_HEAD_DIM) return KATTN_ERR_UNSUPPORTED;
+  if (row_stride_elems < (int64_t)n_kv * d) return KATTN_ERR_INVALID_ARG;
+  if (n_rows == 0) return KATTN_OK;
+  if (!x || !dst_rows || !out_q || !out_scale) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || row_stride_elems % 4 != 0 || !aligned(dst_rows, 8) ||
+      !aligned(out_q, 16) || !aligned(out_scale, 4))
+    return KATTN_ERR_MISALIGNED;
+  cudaError_t e = launch_quantize_kv(x, n_rows, n_kv, row_stride_elems, out_q, out_scale, 0,
+                                     dst_rows, cap_rows, as_stream(stream));
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+}
+
+int kattn_decode(const float* q, const int8_t* k, const float* k_scale, const int8_t* v,
+                 const float* v_scale, const int64_t* row_start, const int32_t* ctx_len,
+                 int B, int M, int Hq, int Hkv, int d, int cap_rows, int max_ctx,
+                 float sm_scale, int p_mode, int exact_mode, float* out, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  int st = check_common(q, k, k_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
+  if (st != KATTN_OK) return st;
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X448) return KATTN_ERR_INVALID_ARG;
+  if (exact_mode != 0 && exact_mode != 1) return KATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
+  if (B == 0) return KATTN_OK;
+  if (!v || !v_scale || !out) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(v, 16) || !aligned(v_scale, 4) || !aligned(out, 16)) return KATTN_ERR_MISALIGNED;
+
+  DecodeParams p = make_params(q, k, k_scale, v, v_scale, row_start, ctx_len, B, M, Hq, Hkv,
+                               cap_rows, max_ctx, sm_scale, p_mode, out);
+  cudaError_t e;
+  if (exact_mode) {
+    e = launch_decode_exact(p, expf_constants(), as_stream(stream));
+  } else {
+    const WorkspaceLayout w = workspace_layout(B, M, Hq, max_ctx);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
+      return KATTN_ERR_WORKSPACE;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    p.err_word = reinterpret_cast<uint32_t*>(ws);
+    p.tickets = reinterpret_cast<uint32_t*>(ws + w.tickets_off);
+    p.partials = reinterpret_cast<float*>(ws + w.partials_off);
+    e = launch_decode_fast(p, as_stream(stream));
+  }
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+}
+
+int kattn_qk_scores_debug(const float* q, const int8_t* k, const float* k_scale,
+                          const int64_t* row_start, const int32_t* ctx_len, int B, int M,
+                          int Hq, int Hkv, int d, int cap_rows, int max_ctx, int32_t* scores,
+                          int8_t* q_i8, float* q_scale, void* stream) {
+  int st = check_common(q, k, k_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
+  if (st != KATTN_OK) return st;
+  if (B == 0) return KATTN_OK;
+  if (!scores) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(scores, 4) || (q_i8 && !aligned(q_i8, 16)) || (q_scale && !aligned(q_scale, 4)))
+    return KATTN_ERR_MISALIGNED;
+  DecodeParams p = make_params(q, k, k_scale, nullptr, nullptr, row_start, ctx_len, B, M, Hq,
+                               Hkv, cap_rows, max_ctx, 0.0f, 0, nullptr);
+  cudaError_t e = launch_qk_debug(p, scores, q_i8, q_scale, as_stream(stream));
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+}
+
+int kattn_get_device_status(void* workspace, size_t workspace_bytes, int* device_err,
+                            void* stream) {
+  if (!workspace || !device_err || workspace_bytes < 256) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return KATTN_ERR_WORKSPACE;
+  uint32_t word = 0;
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KATTN_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return KATTN_ERR_CUDA;
+  *device_err = (int)word;
+  return KATTN_OK;
+}
+
+}  // extern "C"

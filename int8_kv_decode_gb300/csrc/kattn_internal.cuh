@@ -1,0 +1,84 @@
+// Internal declarations shared by the kattn CUDA translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kattn.h"
+
+namespace kattn {
+
+constexpr int kD = KATTN_HEAD_DIM;    // head_dim
+constexpr int kSplitC = 512;          // keys per split (fixed: batch invariance)
+constexpr int kTileBk = 64;           // keys per online-softmax block
+constexpr int kMaxRows = KATTN_MAX_ROWS;
+constexpr int kMaxM = KATTN_MAX_M;
+static_assert(kSplitC % kTileBk == 0, "a split is a whole number of blocks");
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- workspace
+// [0, 256)                   header: uint32 error word at offset 0
+// [256, 256 + T)             uint32 tickets, one per (b, kv head) -- B*Hq slots
+// [P0, ...)                  float partials per (b, split, kv head):
+//                            o[R][d], then m[R], then l[R]   (R = g*M rows)
+struct WorkspaceLayout {
+  size_t tickets_off;
+  size_t partials_off;
+  size_t total;
+  int nsplit_max;
+};
+
+__host__ __device__ inline int nsplit_for(int keys) { return (keys + kSplitC - 1) / kSplitC; }
+
+inline WorkspaceLayout workspace_layout(int B, int M, int Hq, int max_ctx) {
+  WorkspaceLayout w{};
+  w.nsplit_max = nsplit_for(max_ctx + M - 1);
+  w.tickets_off = 256;
+  size_t tick = (size_t)B * (size_t)Hq * sizeof(uint32_t);
+  w.partials_off = (w.tickets_off + tick + 255) / 256 * 256;
+  size_t part = (size_t)B * (size_t)w.nsplit_max * (size_t)Hq * (size_t)M *
+                (size_t)(kD + 2) * sizeof(float);
+  w.total = (w.partials_off + part + 255) / 256 * 256;
+  return w;
+}
+
+struct DecodeParams {
+  const float* q;
+  const int8_t* k;
+  const float* k_scale;
+  const int8_t* v;
+  const float* v_scale;
+  const int64_t* row_start;
+  const int32_t* ctx_len;
+  float* out;
+  uint32_t* err_word;   // workspace header (fast mode), may be null in exact mode
+  uint32_t* tickets;    // [B][Hkv]
+  float* partials;
+  int B, M, Hq, Hkv, g, R;
+  int cap_rows, max_ctx, nsplit_max;
+  float sm_scale;       // already resolved (never 0)
+  int p_mode;
+};
+
+// Constants of the table-driven exp used by exact mode; computed on the host
+// from first principles (see expf_constants.cpp) and passed by value.
+struct ExpfConsts {
+  double K, C2, C0, C1;
+  double T[64];
+};
+
+const ExpfConsts& expf_constants();
+
+// Launchers (return a cudaError_t of the launch).
+cudaError_t launch_quantize_kv(const float* x, int n_rows, int n_kv, int64_t row_stride,
+                               int8_t* out_q, float* out_scale, int64_t dst_row0,
+                               const int64_t* dst_rows, int cap_rows, cudaStream_t stream);
+cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_exact(const DecodeParams& p, const ExpfConsts& c,
+                                cudaStream_t stream);
+cudaError_t launch_qk_debug(const DecodeParams& p, int32_t* scores, int8_t* q_i8,
+                            float* q_scale, cudaStream_t stream);
+
+}  // namespace kattn

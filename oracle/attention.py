@@ -158,10 +158,13 @@ def _check(q, k8, ks, v8, vs, row_start, ctx):
     return B, M, Hq, Hkv, d
 
 
+NO_SCORE = np.iinfo(np.int64).min   # cannot be a score: |S| <= 128 * 127^2
+
+
 def qk_scores(q, k8, row_start, ctx):
     """Reference for the QK debug entry point.
 
-    Returns (S int64 [B][M][Hq][max_ctx + M - 1] with -1 sentinels where
+    Returns (S int64 [B][M][Hq][max_ctx + M - 1] holding NO_SCORE where
     t >= L_j, q8 int8 [B][M][Hq][d], qs float32 [B][M][Hq]).
     """
     q = np.asarray(q, np.float32)
@@ -169,7 +172,7 @@ def qk_scores(q, k8, row_start, ctx):
     g = Hq // Hkv
     q8, qs = quantize_queries(q)
     width = int(np.max(ctx)) + M - 1
-    S = np.full((B, M, Hq, width), -1, dtype=np.int64)
+    S = np.full((B, M, Hq, width), NO_SCORE, dtype=np.int64)
     for b in range(B):
         for j in range(M):
             L = int(ctx[b]) + j

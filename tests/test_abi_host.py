@@ -1,0 +1,132 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/kattn.h declares, and rejects bad arguments on the host before
+anything is launched.  No test here passes validation, so nothing runs on a
+device.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "kattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from int8_kv_decode_gb300 import _lib
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kattn_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    from int8_kv_decode_gb300 import _lib
+    assert sorted(_lib.SIGNATURES) == names      # binding covers the header exactly
+
+
+def test_status_strings(lib):
+    assert lib.kattn_status_string(0) == b"KATTN_OK"
+    assert lib.kattn_status_string(-3) == b"KATTN_ERR_MISALIGNED"
+    assert lib.kattn_status_string(123) == b"KATTN_UNKNOWN_STATUS"
+
+
+def test_tiling(lib):
+    c, bk = ctypes.c_int(), ctypes.c_int()
+    assert lib.kattn_get_tiling(ctypes.byref(c), ctypes.byref(bk)) == 0
+    assert c.value % bk.value == 0 and c.value >= bk.value
+    assert lib.kattn_get_tiling(None, None) == 0
+
+
+def test_workspace_size(lib):
+    c = ctypes.c_int()
+    lib.kattn_get_tiling(ctypes.byref(c), None)
+    C = c.value
+    n = lib.kattn_decode_workspace_size(4, 1, 32, 8192)
+    nsplit = (8192 + C - 1) // C
+    assert n >= 4 * nsplit * 32 * (128 + 2) * 4
+    assert n % 256 == 0
+    assert lib.kattn_decode_workspace_size(0, 1, 32, 8192) == 0
+    assert lib.kattn_decode_workspace_size(1, 9, 32, 8192) == 0
+    assert lib.kattn_decode_workspace_size(4, 5, 32, 8192) > n
+
+
+def test_expf_constants_match_oracle(lib):
+    # The library derives its constants in double-double arithmetic; the
+    # oracle uses the decimal module.  Independent derivations must agree.
+    from oracle import expf_tang as E
+    buf = (ctypes.c_double * 68)()
+    assert lib.kattn_expf_constants(buf) == 0
+    got = list(buf)
+    assert got[:4] == [E.K, E.C2, E.C0, E.C1]
+    assert got[4:] == list(E.TABLE)
+    assert lib.kattn_expf_constants(None) == -1
+
+
+def _decode(lib, **kw):
+    a = dict(q=64, k=64, ks=64, v=64, vs=64, rs=64, ctx=64, B=1, M=1, Hq=8, Hkv=2, d=128,
+             cap=256, max_ctx=256, sm=0.0, p_mode=0, exact=0, out=64, ws=0, ws_bytes=0,
+             stream=0)
+    a.update(kw)
+    return lib.kattn_decode(a["q"], a["k"], a["ks"], a["v"], a["vs"], a["rs"], a["ctx"],
+                            a["B"], a["M"], a["Hq"], a["Hkv"], a["d"], a["cap"], a["max_ctx"],
+                            a["sm"], a["p_mode"], a["exact"], a["out"], a["ws"], a["ws_bytes"],
+                            a["stream"])
+
+
+def test_decode_validation(lib):
+    INVALID, UNSUP, MISAL, WS = -1, -2, -3, -4
+    assert _decode(lib, q=0) == INVALID
+    assert _decode(lib, Hq=6, Hkv=4) == INVALID
+    assert _decode(lib, d=64) == UNSUP
+    assert _decode(lib, M=9) == UNSUP
+    assert _decode(lib, Hq=128, Hkv=1, M=1) == UNSUP       # g*M = 128 > 64
+    assert _decode(lib, q=0x1008) == MISAL
+    assert _decode(lib, k=0x1004) == MISAL
+    assert _decode(lib, rs=0x1004) == MISAL
+    assert _decode(lib, p_mode=4) == INVALID
+    assert _decode(lib, exact=2) == INVALID
+    assert _decode(lib, sm=float("nan")) == INVALID
+    assert _decode(lib, max_ctx=0) == INVALID
+    assert _decode(lib, cap=0) == INVALID
+    assert _decode(lib, ws=0) == WS                        # fast mode needs one
+    assert _decode(lib, ws=0x1100, ws_bytes=16) == WS      # too small
+    assert _decode(lib, ws=0x1010, ws_bytes=1 << 30) == WS  # not 256-aligned
+    assert _decode(lib, B=0) == 0                          # empty batch: no-op
+
+
+def test_quantize_validation(lib):
+    f = lib.kattn_quantize_kv
+    assert f(64, 4, 2, 64, 256, 64, 64, 0, 8, 0) == -2       # d != 128
+    assert f(64, 4, 2, 128, 255, 64, 64, 0, 8, 0) == -1      # stride < n_kv*d
+    assert f(64, 4, 2, 128, 258, 64, 64, 0, 8, 0) == -3      # stride not /4
+    assert f(64, 4, 2, 128, 256, 64, 64, 6, 8, 0) == -1      # dst_row0 + n > cap
+    assert f(0, 4, 2, 128, 256, 64, 64, 0, 8, 0) == -1       # null x
+    assert f(64, 0, 2, 128, 256, 64, 64, 0, 8, 0) == 0       # no rows: no-op
+
+
+def test_qk_debug_validation(lib):
+    f = lib.kattn_qk_scores_debug
+    assert f(64, 64, 64, 64, 64, 1, 1, 8, 2, 128, 256, 256, 0, 0, 0, 0) == -1   # scores null
+    assert f(64, 64, 64, 64, 64, 1, 1, 8, 2, 128, 256, 256, 0x1002, 0, 0, 0) == -3
+    assert f(64, 64, 64, 64, 64, 1, 1, 8, 2, 96, 256, 256, 64, 0, 0, 0) == -2
+
+
+def test_device_status_validation(lib):
+    err = ctypes.c_int()
+    assert lib.kattn_get_device_status(None, 1024, ctypes.byref(err), None) == -1
+    assert lib.kattn_get_device_status(0x1010, 1024, ctypes.byref(err), None) == -4

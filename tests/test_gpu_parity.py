@@ -1,0 +1,298 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars: bit-exact for quantized bytes, integer QK scores and exact mode;
+max|delta| <= 1e-4 and relative L2 <= 1e-5 for fast mode with f32 P;
+relative L2 <= 2e-3 for the rounded-P modes against the oracle applying the
+same rounding at the same points; bit-identical run to run and across
+columns / batch sizes.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from helpers import (ROUNDED_REL_L2, assert_f32_tolerance, custom, oracle_decode, rel_l2,
+                     row_mask, run, sample_rows, upload)
+from synth import WORKLOADS, make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def bits(a):
+    return np.ascontiguousarray(np.asarray(a, np.float32)).view(np.uint32)
+
+
+# ----------------------------------------------------------- quantization --
+
+@pytest.mark.parametrize("name", ["tiny", "qwen_layer", "spec_verify"])
+def test_quantize_kv_bytes(name):
+    c = upload(WORKLOADS[name])
+    assert np.array_equal(c.k8.cpu().numpy(), c.ok8)
+    assert np.array_equal(c.v8.cpu().numpy(), c.ov8)
+    assert np.array_equal(bits(c.ks.cpu()), bits(c.oks))
+    assert np.array_equal(bits(c.vs.cpu()), bits(c.ovs))
+
+
+def test_quantize_kv_offset_zero_rows_and_ties():
+    import torch
+    import int8_kv_decode_gb300 as K
+    rng = np.random.default_rng(5)
+    rows = rng.standard_normal((9, 3, 128)).astype(np.float32)
+    rows[2, 1] = 0.0                               # zero row -> scale 0, zeros
+    rows[4, 0] = 0.0
+    rows[4, 0, :6] = [127, 2.5, -2.5, 3.5, 0.5, -1.5]   # scale exactly 1: ties
+    cap, r0 = 20, 7
+    q8 = torch.full((3, cap, 128), 99, dtype=torch.int8, device="cuda")
+    sc = torch.full((3, cap), -1.0, dtype=torch.float32, device="cuda")
+    K.quantize_kv(torch.from_numpy(rows).cuda(), q8, sc, dst_row0=r0)
+    oq, os_ = oracle.quant.quantize_kv(rows)
+    assert np.array_equal(q8.cpu().numpy()[:, r0:r0 + 9], oq)
+    assert np.array_equal(bits(sc.cpu().numpy()[:, r0:r0 + 9]), bits(os_))
+    assert (q8.cpu().numpy()[:, :r0] == 99).all() and (q8.cpu().numpy()[:, r0 + 9:] == 99).all()
+    assert list(q8.cpu().numpy()[0, r0 + 4, :6]) == [127, 2, -2, 4, 0, -2]
+
+
+# --------------------------------------------------------------- QK scores --
+
+@pytest.mark.parametrize("name", ["tiny", "qwen_layer", "spec_verify"])
+def test_qk_scores_bit_exact(name):
+    import int8_kv_decode_gb300 as K
+    c = upload(WORKLOADS[name])
+    S, q8, qs = K.qk_scores_debug(c.q, c.k8, c.ks, c.rs, c.ctx, c.x.max_ctx, want_q=True)
+    S = S.cpu().numpy()
+    oS, oq8, oqs = oracle.attention.qk_scores(c.x.q, c.ok8, c.x.row_start, c.x.ctx)
+    valid = oS != oracle.attention.NO_SCORE
+    assert np.array_equal(S[valid], oS[valid].astype(np.int32))
+    assert np.all(S[~valid] == -2 ** 31)          # entries t >= L_j untouched
+    assert np.array_equal(q8.cpu().numpy(), oq8)
+    assert np.array_equal(bits(qs.cpu()), bits(oqs))
+
+
+# -------------------------------------------------------------- exact mode --
+
+@pytest.mark.parametrize("name,p_mode", [("tiny", 0), ("tiny", 1), ("tiny", 2), ("tiny", 3),
+                                         ("qwen_layer", 0), ("qwen_layer", 3)])
+def test_exact_mode_bit_exact(name, p_mode):
+    c = upload(WORKLOADS[name])
+    got = run(c, exact_mode=True, p_mode=p_mode).cpu().numpy()
+    ref = oracle_decode(c, mode="exact", p_mode=p_mode)
+    assert np.array_equal(bits(got), bits(ref))
+
+
+def test_exact_mode_spec_verify_sampled():
+    c = upload(WORKLOADS["spec_verify"])
+    got = run(c, exact_mode=True).cpu().numpy()
+    rows = [(b, j, h) for b in (0, 15) for j in range(5) for h in (0, 3, 29)]
+    ref = oracle_decode(c, mode="exact", rows=rows)
+    m = row_mask(got.shape, rows)
+    assert np.array_equal(bits(got[m]), bits(ref[m]))
+
+
+# --------------------------------------------------------------- fast mode --
+
+@pytest.mark.parametrize("name", ["tiny", "qwen_layer"])
+def test_fast_f32_within_tolerance(name):
+    c = upload(WORKLOADS[name])
+    got = run(c).cpu().numpy()
+    assert_f32_tolerance(got, oracle_decode(c))
+
+
+def test_fast_f32_spec_verify_sampled():
+    c = upload(WORKLOADS["spec_verify"])
+    got = run(c).cpu().numpy()
+    rows = sample_rows(c.x, 60, seed=1)
+    ref = oracle_decode(c, rows=rows)
+    assert_f32_tolerance(got, ref, row_mask(got.shape, rows))
+
+
+@pytest.mark.parametrize("p_mode", [1, 2, 3])
+@pytest.mark.parametrize("name", ["tiny", "qwen_layer"])
+def test_fast_rounded_p_modes(name, p_mode):
+    import int8_kv_decode_gb300 as K
+    C, Bk = K.get_tiling()
+    c = upload(WORKLOADS[name])
+    got = run(c, p_mode=p_mode).cpu().numpy()
+    same = oracle_decode(c, p_mode=p_mode, C=C, Bk=Bk)
+    assert rel_l2(got, same) <= ROUNDED_REL_L2
+    if p_mode in (1, 2):
+        # the rounding is really applied: much closer to the same-rounding
+        # oracle than to the unrounded one
+        assert rel_l2(got, same) < 0.5 * rel_l2(got, oracle_decode(c))
+
+
+def test_fast_deterministic_run_to_run():
+    c = upload(WORKLOADS["spec_verify"])
+    for p_mode in (0, 2):
+        a = run(c, p_mode=p_mode).cpu().numpy()
+        for _ in range(2):
+            assert np.array_equal(bits(run(c, p_mode=p_mode).cpu().numpy()), bits(a))
+
+
+@pytest.mark.parametrize("exact", [False, True])
+def test_columns_equal_single_column_decodes(exact):
+    # "Kestrel_VLLM - 18" §二: batch-verify column j must equal, byte for
+    # byte, an M=1 decode that saw the same tokens (ctx + j keys).
+    import int8_kv_decode_gb300 as K
+    c = upload(WORKLOADS["spec_verify"])
+    full = run(c, exact_mode=exact).cpu().numpy()
+    for j in range(c.x.wl.M):
+        qj = c.q[:, j:j + 1].contiguous()
+        one = K.decode(qj, c.k8, c.ks, c.v8, c.vs, c.rs, c.ctx + j, c.x.max_ctx + j,
+                       exact_mode=exact).cpu().numpy()
+        assert np.array_equal(bits(full[:, j:j + 1]), bits(one)), j
+
+
+def test_batch_size_invariance():
+    import torch
+    import int8_kv_decode_gb300 as K
+    wl = WORKLOADS["serving_b64_m4"]
+    x = make_workload(wl, device="cuda")
+    k8 = torch.empty((wl.Hkv, x.cap_rows, wl.d), dtype=torch.int8, device="cuda")
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((wl.Hkv, x.cap_rows), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    K.quantize_kv(x.k_rows, k8, ks)
+    K.quantize_kv(x.v_rows, v8, vs)
+    rs = torch.from_numpy(x.row_start).cuda()
+    ctx = torch.from_numpy(x.ctx).cuda()
+    full = K.decode(x.q, k8, ks, v8, vs, rs, ctx, x.max_ctx).cpu().numpy()
+    for lo, hi in ((0, 1), (5, 9), (10, 26), (63, 64)):
+        sub = K.decode(x.q[lo:hi].contiguous(), k8, ks, v8, vs, rs[lo:hi].contiguous(),
+                       ctx[lo:hi].contiguous(), int(x.ctx[lo:hi].max()) + 7).cpu().numpy()
+        assert np.array_equal(bits(full[lo:hi]), bits(sub)), (lo, hi)
+    # the same sequence moved to another place in another cache
+    b = 11
+    r0, r1 = x.rows_of(b)
+    n = r1 - r0
+    k2 = torch.zeros((wl.Hkv, n + 37, wl.d), dtype=torch.int8, device="cuda")
+    v2, ks2, vs2 = torch.zeros_like(k2), torch.zeros((wl.Hkv, n + 37), device="cuda"), None
+    vs2 = torch.zeros_like(ks2)
+    k2[:, 37:] = k8[:, r0:r1]
+    v2[:, 37:] = v8[:, r0:r1]
+    ks2[:, 37:] = ks[:, r0:r1]
+    vs2[:, 37:] = vs[:, r0:r1]
+    one = K.decode(x.q[b:b + 1].contiguous(), k2, ks2, v2, vs2,
+                   torch.tensor([37], dtype=torch.int64, device="cuda"),
+                   ctx[b:b + 1].contiguous(), int(x.ctx[b])).cpu().numpy()
+    assert np.array_equal(bits(full[b:b + 1]), bits(one))
+
+
+@pytest.mark.parametrize("g,M", [(1, 1), (4, 1), (8, 1), (1, 8), (4, 3), (8, 2), (8, 5), (8, 8)])
+def test_shape_sweep(g, M):
+    # ctx around the block and split sizes ("海光 DCU 实测" §4: one shape being
+    # exact proves nothing about the others).
+    import int8_kv_decode_gb300 as K
+    C, Bk = K.get_tiling()
+    ctxs = np.array([1, 2, Bk - 1, Bk, Bk + 1, C - 1, C, C + 1, 2 * C + 3], np.int32)
+    wl = custom(f"sweep_g{g}_m{M}", len(ctxs), M, 2 * g, 2, 1, outliers=True)
+    c = upload(wl, ctx_override=ctxs)
+    got = run(c).cpu().numpy()
+    assert_f32_tolerance(got, oracle_decode(c))
+    for j in range(M):
+        one = K.decode(c.q[:, j:j + 1].contiguous(), c.k8, c.ks, c.v8, c.vs, c.rs, c.ctx + j,
+                       c.x.max_ctx + j).cpu().numpy()
+        assert np.array_equal(bits(got[:, j:j + 1]), bits(one))
+    ex = run(c, exact_mode=True, p_mode=2).cpu().numpy()
+    rows = [(b, j, h) for b in range(len(ctxs)) for j in (0, M - 1) for h in (0, 2 * g - 1)]
+    ref = oracle_decode(c, mode="exact", p_mode=2, rows=rows)
+    m = row_mask(ex.shape, rows)
+    assert np.array_equal(bits(ex[m]), bits(ref[m]))
+
+
+def test_bad_sequence_is_flagged_without_touching_other_rows():
+    import torch
+    import int8_kv_decode_gb300 as K
+    wl = custom("bad", 3, 2, 8, 2, 300, outliers=False)
+    c = upload(wl)
+    clean = run(c).cpu().numpy()
+    ws = K.alloc_workspace(3, 2, 8, c.x.max_ctx)
+    assert K.get_device_status(ws) == 0
+    bad_ctx = c.ctx.clone()
+    bad_ctx[1] = c.x.max_ctx + 1                       # breaks ctx <= max_ctx
+    out = K.decode(c.q, c.k8, c.ks, c.v8, c.vs, c.rs, bad_ctx, c.x.max_ctx,
+                   workspace=ws).cpu().numpy()
+    assert np.isnan(out[1]).all()
+    assert np.array_equal(bits(out[[0, 2]]), bits(clean[[0, 2]]))
+    assert K.get_device_status(ws) == 1
+    assert K.get_device_status(ws) == 0                # the read cleared it
+    bad_rs = c.rs.clone()
+    bad_rs[2] = c.x.cap_rows                           # rows past the cache
+    ex = K.decode(c.q, c.k8, c.ks, c.v8, c.vs, bad_rs, c.ctx, c.x.max_ctx,
+                  exact_mode=True).cpu().numpy()
+    assert np.isnan(ex[2]).all() and np.isfinite(ex[:2]).all()
+    torch.cuda.synchronize()
+
+
+# -------------------------------------------------------------- full size --
+
+def _device_case(name):
+    import torch
+    import int8_kv_decode_gb300 as K
+    wl = WORKLOADS[name]
+    x = make_workload(wl, device="cuda")
+    k8 = torch.empty((wl.Hkv, x.cap_rows, wl.d), dtype=torch.int8, device="cuda")
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((wl.Hkv, x.cap_rows), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    K.quantize_kv(x.k_rows, k8, ks)
+    K.quantize_kv(x.v_rows, v8, vs)
+    return x, k8, ks, v8, vs
+
+
+def _oracle_one_sequence(x, b, rows, k8, ks, **kw):
+    """Oracle on sequence b alone, from the generator's float32 rows."""
+    lo, hi = x.rows_of(b)
+    kr = x.k_rows[lo:hi].cpu().numpy()
+    vr = x.v_rows[lo:hi].cpu().numpy()
+    ok8, oks = oracle.quant.quantize_kv(kr)
+    ov8, ovs = oracle.quant.quantize_kv(vr)
+    assert np.array_equal(k8[:, lo:hi].cpu().numpy(), ok8)      # quantization parity
+    assert np.array_equal(bits(ks[:, lo:hi].cpu().numpy()), bits(oks))
+    q = x.q[b:b + 1].cpu().numpy()
+    return oracle.attention.decode(q, ok8, oks, ov8, ovs, np.array([0]), x.ctx[b:b + 1],
+                                   rows=[(0, j, h) for (j, h) in rows], **kw)
+
+
+@pytest.mark.parametrize("p_mode", [0, 2])
+def test_full_size_long_context_sampled(p_mode):
+    import torch
+    import int8_kv_decode_gb300 as K
+    C, Bk = K.get_tiling()
+    x, k8, ks, v8, vs = _device_case("long_128k")
+    out = K.decode(x.q, k8, ks, v8, vs, torch.from_numpy(x.row_start).cuda(),
+                   torch.from_numpy(x.ctx).cuda(), x.max_ctx, p_mode=p_mode).cpu().numpy()
+    assert np.isfinite(out).all()
+    got, ref = [], []
+    for b, rows in ((0, [(0, 0), (0, 31)]), (3, [(0, 17)])):
+        o = _oracle_one_sequence(x, b, rows, k8, ks, p_mode=p_mode, C=C, Bk=Bk)
+        for (j, h) in rows:
+            got.append(out[b, j, h])
+            ref.append(o[0, j, h])
+    if p_mode == 0:
+        assert_f32_tolerance(np.array(got), np.array(ref))
+    else:
+        assert rel_l2(np.array(got), np.array(ref)) <= ROUNDED_REL_L2
+
+
+def test_full_size_serving_sampled():
+    import torch
+    import int8_kv_decode_gb300 as K
+    x, k8, ks, v8, vs = _device_case("serving_b256_m1")
+    out = K.decode(x.q, k8, ks, v8, vs, torch.from_numpy(x.row_start).cuda(),
+                   torch.from_numpy(x.ctx).cuda(), x.max_ctx).cpu().numpy()
+    assert np.isfinite(out).all()
+    got, ref = [], []
+    longest = int(np.argmax(x.ctx))
+    for b in (0, longest, 255):
+        rows = [(0, 0), (0, 31)]
+        o = _oracle_one_sequence(x, b, rows, k8, ks)
+        for (j, h) in rows:
+            got.append(out[b, j, h])
+            ref.append(o[0, j, h])
+    assert_f32_tolerance(np.array(got), np.array(ref))

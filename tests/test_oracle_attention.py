@@ -64,7 +64,7 @@ def test_qk_scores_layout_and_gqa():
             for h in range(Hq):
                 for t in range(S.shape[-1]):
                     if t >= L:
-                        assert S[b, j, h, t] == -1
+                        assert S[b, j, h, t] == A.NO_SCORE
                         continue
                     row = k8[h // g, rs[b] + t]
                     assert S[b, j, h, t] == sum(int(x) * int(y) for x, y in zip(q8[b, j, h], row))
