@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Decode-attention benchmark: KV GB/s and queries/s on GB300, % of HBM roofline.
+
+One step = one decode step of the hot path over one batch of synthetic
+sequences: quantize this step's appended K and V rows into the int8 cache
+(one scatter launch each) and run kattn_decode over every sequence.  The
+default workload is the serving mix: 256 ragged sequences, contexts
+log-uniform in [512, 32768], 32 query / 4 KV heads, head_dim 128, M = 1,
+float32 P, fast mode.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+With N > 1 (torchrun, one rank per GPU) every rank decodes its own batch
+(weak scaling, no data-path collective); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "serving_b256_m1"
+METRIC = "decode_attn_kv_GBps"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES_NOMINAL = 129 * 1024 * 1024
+HEAD_DIM = 128
+KERNEL_SOURCES = ["decode_fast.cu", "device_common.cuh", "kattn_internal.cuh"]
+
+
+# ------------------------------------------------------------ accounting --
+
+def kv_bytes(ctx, M: int, Hkv: int, d: int = HEAD_DIM) -> int:
+    """Algorithmic KV bytes of one decode call: every visible (key, kv head)
+    row once -- int8 K and V rows plus their two float32 scales."""
+    return int(sum(Hkv * (int(c) + M - 1) * (2 * d + 8) for c in ctx))
+
+
+def qo_bytes(B: int, M: int, Hq: int, d: int = HEAD_DIM) -> int:
+    """float32 queries read plus float32 outputs written."""
+    return 2 * B * M * Hq * d * 4
+
+
+def append_rows(row_start, ctx, M: int):
+    """Cache rows written by this step: the M newest rows of each sequence
+    (draft column j's own key is row ctx + j - 1)."""
+    rows = []
+    for rs, c in zip(row_start, ctx):
+        rows.extend(int(rs) + int(c) - 1 + j for j in range(M))
+    return rows
+
+
+def load_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "int8_kv_decode_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, sha: str):
+    """DRAM bytes per launch of the decode kernel from a committed ncu summary
+    line 'traffic_per_launch <workload> <source sha> <bytes>', if the kernel
+    sources are unchanged since the capture; else None."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name), encoding="utf-8") as f:
+            for line in f:
+                parts = line.strip().strip("`").split()
+                if len(parts) == 4 and parts[0] == "traffic_per_launch" \
+                        and parts[1] == workload and parts[2] == sha:
+                    return float(parts[3])
+    return None
+
+
+# ------------------------------------------------------------- clocks ----
+
+CLOCK_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                "clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def start_clock_sampler(gpu_id: str, path: str, period_ms: int = 20):
+    try:
+        f = open(path, "w")
+        p = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                              "-i", gpu_id, "-lms", str(period_ms)], stdout=f,
+                             stderr=subprocess.DEVNULL)
+        return p, f
+    except OSError:
+        return None, None
+
+
+def stop_clock_sampler(handle):
+    p, f = handle
+    if p is not None:
+        p.terminate()
+        try:
+            p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            p.kill()
+    if f is not None:
+        f.close()
+
+
+def parse_clocks(text: str, t0: float = None, t1: float = None):
+    """Summarise nvidia-smi samples (CSV, no header, no units).  Samples whose
+    timestamp falls in [t0, t1] (epoch seconds) are used when there are any;
+    otherwise all samples are."""
+    rows = []
+    for line in text.splitlines():
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) != 8:
+            continue
+        try:
+            ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            rows.append((ts + frac, float(parts[1]), float(parts[2]), parts[4:]))
+        except (ValueError, IndexError):
+            continue
+    if not rows:
+        return None
+    inside = [r for r in rows if t0 is not None and t0 - 0.05 <= r[0] <= t1 + 0.05]
+    use = inside or rows
+    reasons = sorted({REASON_NAMES[i] for r in use for i, v in enumerate(r[3])
+                      if v.lower().startswith("active")})
+    return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+            "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside)}
+
+
+# --------------------------------------------------------- distribution --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(local_bytes: float, local_queries: float, local_seconds: float, pg=None):
+    """Whole-job totals: bytes and queries summed over ranks, time = max over
+    ranks (the slowest rank bounds the job)."""
+    if pg is None:
+        return local_bytes, local_queries, local_seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_bytes, local_queries], dtype=torch.float64)
+    m = torch.tensor([local_seconds], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t, m = t.cuda(), m.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    return float(t[0]), float(t[1]), float(m[0])
+
+
+# ---------------------------------------------------------------- oracle --
+
+def oracle_sample(wl, n_seq: int, seed_rep: int = 0):
+    """Host inputs for the first n_seq context lengths of the workload (same
+    length draw, fresh host values), quantized by the oracle."""
+    import numpy as np
+    import oracle
+    from synth import make_lengths, make_workload
+    import dataclasses
+    rng = np.random.Generator(np.random.PCG64(wl.index * 1000 + seed_rep))
+    ctx = make_lengths(wl, rng)[:n_seq]
+    small = dataclasses.replace(wl, B=len(ctx))
+    x = make_workload(small, rep=seed_rep, ctx_override=ctx)
+    k8, ks = oracle.quant.quantize_kv(x.k_rows)
+    v8, vs = oracle.quant.quantize_kv(x.v_rows)
+    return x, (k8, ks, v8, vs)
+
+
+def time_oracle(wl, budget_s: float, max_seq: int = 12):
+    """Oracle reference decode (float64, f32 P) on whole sequences of the
+    workload until budget_s of CPU time is spent.  Returns (GB/s, queries/s,
+    seconds, sequences, cores)."""
+    import contextlib
+    import oracle
+    try:
+        from threadpoolctl import threadpool_limits
+        limit = threadpool_limits(limits=1)
+    except ImportError:
+        limit = contextlib.nullcontext()
+    x, (k8, ks, v8, vs) = oracle_sample(wl, max_seq)
+    spent = 0.0
+    nbytes = nq = n = 0
+    with limit:
+        for b in range(x.wl.B):
+            t0 = time.perf_counter()
+            oracle.attention.decode(x.q[b:b + 1], k8, ks, v8, vs, x.row_start[b:b + 1],
+                                    x.ctx[b:b + 1])
+            spent += time.perf_counter() - t0
+            nbytes += kv_bytes(x.ctx[b:b + 1], wl.M, wl.Hkv)
+            nq += wl.M
+            n += 1
+            if spent >= budget_s:
+                break
+    return nbytes / spent / 1e9, nq / spent, spent, n, 1
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, timed as it stands, one bounded
+    sample of the workload per step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from synth import WORKLOADS
+    import oracle
+    wl = WORKLOADS[args.workload]
+    x, (k8, ks, v8, vs) = oracle_sample(wl, args.ref_sequences)
+    n_seq = x.wl.B
+    bytes_per_step = kv_bytes(x.ctx, wl.M, wl.Hkv)
+
+    def step():
+        oracle.attention.decode(x.q, k8, ks, v8, vs, x.row_start, x.ctx)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = bytes_per_step / dt / 1e9
+    sample = (f"{n_seq} sequences of the {wl.name} workload (first {n_seq} context lengths, "
+              f"mean {float(x.ctx.mean()):.0f}), float64 reference, f32 P, per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "queries_per_s": n_seq * wl.M / dt,
+        "config": workload_config(wl, x.ctx, note="bounded sample"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, ctx, note=None, l2=None):
+    import numpy as np
+    c = {"workload": wl.name, "B": wl.B, "M": wl.M, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+         "ctx": wl.ctx if isinstance(wl.ctx, int) else f"{wl.ctx[0]}[{wl.ctx[1]},{wl.ctx[2]}]",
+         "mean_ctx": float(np.mean(ctx)), "p_mode": "f32", "exact_mode": False}
+    if l2:
+        c["l2"] = l2
+    if note:
+        c["note"] = note
+    return c
+
+
+# ------------------------------------------------------------------ ours --
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import int8_kv_decode_gb300 as K
+    from synth import WORKLOADS, make_workload
+
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N>1 with torchrun")
+    pg = None
+    if world > 1:
+        dist.init_process_group(backend="nccl")
+        pg = dist.group.WORLD
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K.load()
+
+    wl = WORKLOADS[args.workload]
+    x = make_workload(wl, rep=rank, device=str(dev))
+    B, M, Hq, Hkv, d = wl.B, wl.M, wl.Hq, wl.Hkv, wl.d
+    kvb = kv_bytes(x.ctx, M, Hkv)
+    qob = qo_bytes(B, M, Hq)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or L2_BYTES_NOMINAL
+    n_copies = max(1, math.ceil(3 * l2 / kvb))          # keep every step L2-cold
+    caches = []
+    for _ in range(n_copies):
+        k8 = torch.empty((Hkv, x.cap_rows, d), dtype=torch.int8, device=dev)
+        v8 = torch.empty_like(k8)
+        ks = torch.empty((Hkv, x.cap_rows), dtype=torch.float32, device=dev)
+        vs = torch.empty_like(ks)
+        K.quantize_kv(x.k_rows, k8, ks)                   # the prefill, untimed
+        K.quantize_kv(x.v_rows, v8, vs)
+        caches.append((k8, ks, v8, vs))
+    dst = torch.tensor(append_rows(x.row_start, x.ctx, M), dtype=torch.int64, device=dev)
+    knew = x.k_rows[dst].contiguous()
+    vnew = x.v_rows[dst].contiguous()
+    x.k_rows = x.v_rows = None                          # free the float32 prefill rows
+    torch.cuda.empty_cache()
+    q = x.q.contiguous()
+    rs = torch.from_numpy(x.row_start).to(dev)
+    ctx = torch.from_numpy(x.ctx).to(dev)
+    max_ctx = int(x.ctx.max())
+    ws = K.alloc_workspace(B, M, Hq, max_ctx, dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev0=None, ev1=None):
+        k8, ks, v8, vs = caches[i % n_copies]
+        K.quantize_kv_rows(knew, dst, k8, ks)
+        K.quantize_kv_rows(vnew, dst, v8, vs)
+        if ev0 is not None:
+            ev0.record(stream)
+        K.decode(q, k8, ks, v8, vs, rs, ctx, max_ctx, out=out, workspace=ws)
+        if ev1 is not None:
+            ev1.record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if pg is not None:
+        dist.barrier()
+
+    gpu_id = str(local)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clock_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_rank{rank}.csv")
+    sampler = start_clock_sampler(gpu_id, clock_path) if rank == 0 else (None, None)
+    time.sleep(0.3)                                       # sampler start-up
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    if pg is not None:
+        dist.barrier()
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, *evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if pg is not None:
+        dist.barrier()
+    elapsed = start.elapsed_time(end) / 1e3
+    decode_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3 / args.steps
+    stop_clock_sampler(sampler)
+
+    total_bytes, total_q, tmax = aggregate(kvb * args.steps, B * M * args.steps, elapsed, pg)
+
+    # End to end through the public API: inputs from pinned host memory each
+    # step, the result read back to the host each step.
+    h_q = q.cpu().pin_memory()
+    h_knew, h_vnew = knew.cpu().pin_memory(), vnew.cpu().pin_memory()
+    h_ctx = ctx.cpu().pin_memory()
+    h_dst = dst.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = (h_q.numel() * 4 + h_knew.numel() * 4 + h_vnew.numel() * 4 + h_ctx.numel() * 4
+           + h_dst.numel() * 8)
+    d2h = h_out.numel() * 4
+    torch.cuda.synchronize(dev)
+    if pg is not None:
+        dist.barrier()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for i in range(args.steps):
+        q.copy_(h_q, non_blocking=True)
+        knew.copy_(h_knew, non_blocking=True)
+        vnew.copy_(h_vnew, non_blocking=True)
+        ctx.copy_(h_ctx, non_blocking=True)
+        dst.copy_(h_dst, non_blocking=True)
+        step(i)
+        h_out.copy_(out, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e_elapsed = e_start.elapsed_time(e_end) / 1e3
+    _, _, e_tmax = aggregate(0.0, 0.0, e_elapsed, pg)
+
+    if rank != 0:
+        dist.destroy_process_group() if pg is not None else None
+        return 0
+
+    peak, peak_kind = load_peak_hbm()
+    algo = kvb + qob
+    achieved = algo / decode_s / 1e9
+    sha = kernel_source_sha()
+    clocks = None
+    try:
+        with open(clock_path) as f:
+            clocks = parse_clocks(f.read(), wall0, wall1)
+    except OSError:
+        pass
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, qps, secs, nseq, cores = time_oracle(wl, args.cpu_budget)
+        cpu = {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": (f"{nseq} whole sequences of {wl.name} ({secs:.1f} s single-threaded, "
+                          f"float64 reference, f32 P); GB/s = their KV bytes / time"),
+               "queries_per_s": qps}
+
+    line = {
+        "metric": METRIC, "value": total_bytes / tmax / 1e9, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tmax / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i8/f32", "data": "synthetic",
+        "queries_per_s": total_q / tmax,
+        "config": workload_config(
+            wl, x.ctx, l2=(f"inputs larger than L2: {kvb / 1e9:.2f} GB KV per step x "
+                           f"{n_copies} rotating cache copies vs {l2 / 2**20:.0f} MiB L2")),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": profiled_traffic(wl.name, sha),
+                     "kernel": "decode_fast_kernel", "algorithmic_bytes_per_launch": algo,
+                     "avg_launch_us": decode_s * 1e6, "kernel_source_sha": sha},
+        "kv_frac_of_step": (kvb / (elapsed / args.steps) / 1e9) / peak,
+        "cpu_baseline": cpu,
+        "e2e": {"value": total_bytes / e_tmax / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle CPU time for the cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-sequences", type=int, default=2,
+                    help="sequences per step of the reference arm")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -71,6 +71,8 @@ enum kattn_p_mode {
 
 /* Device error bits reported by kattn_get_device_status. */
 #define KATTN_DEVERR_BAD_SEQUENCE 0x1u /* row_start / ctx_len out of range */
+#define KATTN_DEVERR_TIMEOUT 0x2u      /* a bounded wait for a K/V block ran out;
+                                          the affected outputs are not written */
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* kattn_status_string(int status);
@@ -78,10 +80,10 @@ const char* kattn_status_string(int status);
 /* Fixed tiling of the fast decode path.
  * *split_C: keys per split.  The keys of every sequence are cut into splits
  *   at absolute positions [s*C, (s+1)*C); each split is reduced on its own
- *   and the splits are merged in split order.  C is a compile-time constant,
- *   so the result for a query row depends only on its own keys -- never on
- *   the batch size, M, or other sequences (batch invariance, "Kestrel_VLLM -
- *   18" §二).
+ *   (with its own running max) and the splits are merged in split order.  C
+ *   is a compile-time constant, so the result for a query row depends only
+ *   on its own keys -- never on the batch size, M, or other sequences (batch
+ *   invariance, "Kestrel_VLLM - 18" §二).
  * *round_block_Bk: keys per online-softmax block inside a split; the running
  *   max that a rounded P is taken relative to is updated once per block.
  * Either pointer may be NULL.  Never fails. */

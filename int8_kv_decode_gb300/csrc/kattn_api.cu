@@ -28,6 +28,8 @@ int check_common(const float* q, const int8_t* k, const float* k_scale,
   if (d != KATTN_HEAD_DIM) return KATTN_ERR_UNSUPPORTED;
   if (M > KATTN_MAX_M || (Hq / Hkv) * M > KATTN_MAX_ROWS) return KATTN_ERR_UNSUPPORTED;
   if ((int64_t)max_ctx + M - 1 > (int64_t)INT32_MAX / 2) return KATTN_ERR_INVALID_ARG;
+  // the fast path addresses cache rows of all heads with int32 TMA coordinates
+  if ((int64_t)Hkv * cap_rows > (int64_t)INT32_MAX - 4096) return KATTN_ERR_UNSUPPORTED;
   if (B == 0) return KATTN_OK;
   if (!q || !k || !k_scale || !row_start || !ctx_len) return KATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(k_scale, 4) || !aligned(row_start, 8) ||
@@ -80,8 +82,8 @@ const char* kattn_status_string(int status) {
 }
 
 int kattn_get_tiling(int* split_C, int* round_block_Bk) {
-  if (split_C) *split_C = kSplitC;
-  if (round_block_Bk) *round_block_Bk = kTileBk;
+  if (split_C) *split_C = kSpanC;
+  if (round_block_Bk) *round_block_Bk = kBlockBk;
   return KATTN_OK;
 }
 

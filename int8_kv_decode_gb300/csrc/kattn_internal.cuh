@@ -10,11 +10,18 @@
 namespace kattn {
 
 constexpr int kD = KATTN_HEAD_DIM;    // head_dim
-constexpr int kSplitC = 512;          // keys per split (fixed: batch invariance)
-constexpr int kTileBk = 64;           // keys per online-softmax block
+// Fast-path tiling (fixed at compile time, so a row's result never depends on
+// the batch): keys are cut into spans of kSpanC at absolute positions; one
+// warp reduces a span with its own running max, updated every kBlockBk keys
+// (the rounding points of a rounded P).  A CTA owns kSpansPerCta consecutive
+// spans and merges them; CTAs (windows of kSplitC keys) are merged last.
+constexpr int kSpanC = 128;
+constexpr int kBlockBk = 16;
+constexpr int kSpansPerCta = 4;
+constexpr int kSplitC = kSpanC * kSpansPerCta;   // 512 keys per CTA window
 constexpr int kMaxRows = KATTN_MAX_ROWS;
 constexpr int kMaxM = KATTN_MAX_M;
-static_assert(kSplitC % kTileBk == 0, "a split is a whole number of blocks");
+static_assert(kSpanC % kBlockBk == 0, "a span is a whole number of blocks");
 
 constexpr float kLog2e = 1.4426950408889634f;
 

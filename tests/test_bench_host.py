@@ -1,0 +1,87 @@
+"""Host-side logic of bench.py (no GPU): byte accounting, clock parsing, the
+profile lookup, whole-job aggregation over 2 gloo ranks, and the reference
+arm's JSON line."""
+
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_kv_bytes_and_queries():
+    # 264 bytes per (key, kv head) at d = 128: 2 x 128 int8 + 2 float32 scales
+    assert bench.kv_bytes([1024], 1, 4) == 4 * 1024 * 264
+    assert bench.kv_bytes([10, 20], 3, 2) == 2 * (12 + 22) * 264
+    assert bench.qo_bytes(2, 3, 4) == 2 * 2 * 3 * 4 * 128 * 4
+
+
+def test_append_rows_are_each_columns_own_key():
+    assert bench.append_rows([5, 100], [3, 7], 2) == [7, 8, 106, 107]
+
+
+def test_parse_clocks_window_and_reasons():
+    text = "\n".join([
+        "2026/12/02 10:00:00.100, 1980, 2070, 700.1, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 10:00:01.100, 1900, 2070, 900.0, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 10:00:05.100, 1200, 2070, 300.0, Not Active, Active, Not Active, Not Active",
+    ])
+    import time
+    t0 = time.mktime(time.strptime("2026/12/02 10:00:00", "%Y/%m/%d %H:%M:%S"))
+    c = bench.parse_clocks(text, t0, t0 + 2)
+    assert c["samples"] == 2 and c["in_timed_region"]
+    assert c["sm_mhz"] == 1940 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]
+    assert bench.parse_clocks("garbage") is None
+
+
+def test_profiled_traffic_lookup(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "x.md").write_text(
+        "text\n`traffic_per_launch serving_b256_m1 abc123 2.5e9`\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("serving_b256_m1", "abc123") == 2.5e9
+    assert bench.profiled_traffic("serving_b256_m1", "changed") is None
+
+
+def _agg_worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    res = bench.aggregate(100.0 * (rank + 1), 5.0, 0.5 + rank, dist.group.WORLD)
+    q.put((rank, res))
+    dist.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + (os.getpid() % 1000)
+    procs = [ctx.Process(target=_agg_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    for r in range(2):
+        assert got[r] == (300.0, 10.0, 1.5)     # bytes summed, time = max
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"

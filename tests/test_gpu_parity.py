@@ -120,10 +120,13 @@ def test_fast_rounded_p_modes(name, p_mode):
     got = run(c, p_mode=p_mode).cpu().numpy()
     same = oracle_decode(c, p_mode=p_mode, C=C, Bk=Bk)
     assert rel_l2(got, same) <= ROUNDED_REL_L2
-    if p_mode in (1, 2):
-        # the rounding is really applied: much closer to the same-rounding
-        # oracle than to the unrounded one
-        assert rel_l2(got, same) < 0.5 * rel_l2(got, oracle_decode(c))
+    # Where the rounding moves the result measurably, the kernel must apply
+    # it: its distance to the same-rounding oracle is far below the size of
+    # the rounding's own effect.  (With very peaked attention -- the outlier
+    # channels -- p is ~1 or ~0 and no rounding changes anything.)
+    effect = rel_l2(same, oracle_decode(c))
+    if effect > 1e-5:
+        assert rel_l2(got, same) < 0.25 * effect, (rel_l2(got, same), effect)
 
 
 def test_fast_deterministic_run_to_run():
