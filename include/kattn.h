@@ -163,6 +163,37 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale,
                  int exact_mode, float* out, void* workspace,
                  size_t workspace_bytes, void* stream);
 
+/* Allocation-free form of kattn_decode in fast mode (exact_mode = 0).  The
+ * pages have no counterpart to it: it exists for callers that cannot give the
+ * library a workspace -- an engine whose device memory belongs to its own
+ * arena, a serving loop that must not pay cudaMalloc's latency and implicit
+ * synchronisation between steps, or a plugin interface that receives only
+ * input and output buffers.  The caller passes inputs and outputs exactly as
+ * for kattn_decode; the scratch (merge counters and per-window partials)
+ * lives in one device array of KATTN_NOALLOC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  The call allocates nothing and calls no allocating routine.
+ *   - Limit: calls whose kattn_decode_workspace_size(B, M, Hq, max_ctx)
+ *     exceeds KATTN_NOALLOC_SCRATCH_BYTES are rejected with
+ *     KATTN_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's address on that device
+ *     (with that device current); make that first call before any stream
+ *     capture begins.
+ *   - Each call clears the array's counters on `stream` (cudaMemsetAsync)
+ *     before decoding; the array keeps the rest of the last call's contents.
+ *   - All calls on a device share the one array: calls that overlap on the
+ *     GPU (for example on two streams) race and give undefined results, so
+ *     the caller must order them.
+ *   - Device error bits are not reported (the array is private); sequences
+ *     that break the row_start / ctx_len rule still get NaN outputs.
+ * Arguments, results, determinism and errors otherwise as kattn_decode. */
+#define KATTN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int kattn_decode_noalloc(const float* q, const int8_t* k, const float* k_scale,
+                         const int8_t* v, const float* v_scale, const int64_t* row_start,
+                         const int32_t* ctx_len, int B, int M, int Hq, int Hkv, int d,
+                         int cap_rows, int max_ctx, float sm_scale, int p_mode, float* out,
+                         void* stream);
+
 /* Integer QK scores of the decode path, for parity checks ("Kestrel_VLLM -
  * 18" §3.3: int8 query quantization + int32 QK dot product).
  * scores: int32 [B][M][Hq][max_ctx + M - 1]; entry t of row (b, j, h) is

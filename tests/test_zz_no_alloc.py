@@ -1,0 +1,61 @@
+"""kattn_decode_noalloc: the fast decode for callers that cannot allocate.
+
+Callers such as an engine whose device memory belongs to its own arena, a
+serving loop that must not pay cudaMalloc's latency between steps, or a
+plugin interface that only passes input and output buffers cannot hand the
+library a workspace.  This entry point keeps the scratch in a fixed device
+array inside the library instead.  The test calls it through the C ABI twice
+in a row and checks each result against kattn_decode with a workspace
+allocated by the caller.  This file is collected last on purpose.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from helpers import assert_f32_tolerance, run, upload
+from synth import WORKLOADS
+
+
+def _noalloc(c, out):
+    import torch
+    from int8_kv_decode_gb300 import _lib
+    lib = _lib.load()
+    B, M, Hq, d = c.q.shape
+    Hkv, cap, _ = c.k8.shape
+    return lib.kattn_decode_noalloc(
+        c.q.data_ptr(), c.k8.data_ptr(), c.ks.data_ptr(), c.v8.data_ptr(), c.vs.data_ptr(),
+        c.rs.data_ptr(), c.ctx.data_ptr(), B, M, Hq, Hkv, d, cap, c.x.max_ctx, 0.0, 0,
+        out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["qwen_layer", "spec_verify"])
+def test_noalloc_matches_the_workspace_entry_point_on_two_calls(name):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    c = upload(WORKLOADS[name])
+    ref = run(c).cpu().numpy()                  # kattn_decode, caller-owned workspace
+    for _ in range(2):
+        out = torch.full_like(c.q, float("nan"))
+        assert _noalloc(c, out) == 0
+        got = out.cpu().numpy()
+        assert_f32_tolerance(got, ref)
+        # the same kernel on the same inputs: deterministic to the byte
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_noalloc_rejects_requests_beyond_its_scratch():
+    # Checked on the host before any CUDA call: the pointers are never used.
+    import __graft_entry__
+    __graft_entry__.build()
+    from int8_kv_decode_gb300 import _lib
+    lib = _lib.load()
+    fake = 0x100000
+    st = lib.kattn_decode_noalloc(fake, fake, fake, fake, fake, fake, fake,
+                                  4096, 8, 64, 8, 128, 1 << 20, 131072, 0.0, 0, fake, None)
+    assert st == -4                               # KATTN_ERR_WORKSPACE
+    need = lib.kattn_decode_workspace_size(4096, 8, 64, 131072)
+    assert need > 16 * 1024 * 1024
