@@ -16,7 +16,7 @@ constexpr int kD = KATTN_HEAD_DIM;    // head_dim
 // (the rounding points of a rounded P).  A CTA owns kSpansPerCta consecutive
 // spans and merges them; CTAs (windows of kSplitC keys) are merged last.
 constexpr int kSpanC = 128;
-constexpr int kBlockBk = 16;
+constexpr int kBlockBk = 32;
 constexpr int kSpansPerCta = 4;
 constexpr int kSplitC = kSpanC * kSpansPerCta;   // 512 keys per CTA window
 constexpr int kMaxRows = KATTN_MAX_ROWS;
