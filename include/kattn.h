@@ -92,10 +92,12 @@ int kattn_get_tiling(int* split_C, int* round_block_Bk);
 /* Bytes of workspace kattn_decode needs for these sizes (fast mode; exact
  * mode needs none).  max_ctx is the host-side upper bound on ctx_len.
  * Returns 0 for invalid sizes.  Before the FIRST call with a workspace, the
- * caller must zero it (e.g. cudaMemsetAsync); every completed kattn_decode
- * leaves its counters at zero again, so one workspace may be reused by any
- * number of calls that are ordered on the GPU.  Calls that share a workspace
- * and overlap on the GPU race and give undefined results. */
+ * caller must zero it (e.g. cudaMemsetAsync): its first 256 bytes hold the
+ * device error word, which only kattn_get_device_status clears; the rest
+ * (work list, quantized queries, per-window partials) is written by every
+ * call before it is read.  One workspace may be reused by any number of
+ * calls that are ordered on the GPU.  Calls that share a workspace and
+ * overlap on the GPU race and give undefined results. */
 size_t kattn_decode_workspace_size(int B, int M, int Hq, int max_ctx);
 
 /* Quantize K or V rows into the int8 cache ("Kestrel_VLLM - 18" §四 fields
@@ -145,11 +147,16 @@ int kattn_quantize_kv_rows(const float* x, int n_rows, int n_kv, int d,
  * max_ctx:   host-side upper bound on ctx_len (sizes the grid).
  * sm_scale:  0 selects RN_f32(1/sqrt(d)).
  * p_mode:    a kattn_p_mode.
- * exact_mode = 0 (fast): split-KV over splits of C keys, merged in a fixed
- *   order; float32 throughout; deterministic run to run, and the bytes of
+ * exact_mode = 0 (fast): split-KV over spans of C keys, merged in a fixed
+ *   order; float32 accumulation; deterministic run to run, and the bytes of
  *   out[b][j][h] depend only on that row's own keys, so column j equals an
  *   M=1 call with ctx_len + j, in any batch.  Needs a workspace of
  *   kattn_decode_workspace_size(B, M, Hq, max_ctx) bytes, 256-byte aligned.
+ *   Up to three kernels on `stream` (query packing and work list, the
+ *   split-KV pass, the window merge), chained by programmatic dependent
+ *   launch; the call is capturable in a CUDA graph once a first call on the
+ *   device has run outside capture.
+ *   B * ceil((max_ctx + M - 1) / 512) * Hkv above 2^29 -> KATTN_ERR_UNSUPPORTED.
  * exact_mode = 1: one token at a time in token order; every float32
  *   operation rounded separately (no contraction); exp by the table-driven
  *   method of "Kestrel_VLLM - 18" §3.3 (64-entry 2^(j/64) table, 3-term
@@ -169,9 +176,9 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale,
  * arena, a serving loop that must not pay cudaMalloc's latency and implicit
  * synchronisation between steps, or a plugin interface that receives only
  * input and output buffers.  The caller passes inputs and outputs exactly as
- * for kattn_decode; the scratch (merge counters and per-window partials)
- * lives in one device array of KATTN_NOALLOC_SCRATCH_BYTES inside the
- * library, which every GPU that loads the library holds until the process
+ * for kattn_decode; the scratch (work list, quantized queries and per-window
+ * partials) lives in one device array of KATTN_NOALLOC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until the process
  * exits.  The call allocates nothing and calls no allocating routine.
  *   - Limit: calls whose kattn_decode_workspace_size(B, M, Hq, max_ctx)
  *     exceeds KATTN_NOALLOC_SCRATCH_BYTES are rejected with
@@ -179,7 +186,7 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale,
  *   - The first call on a device looks up the array's address on that device
  *     (with that device current); make that first call before any stream
  *     capture begins.
- *   - Each call clears the array's counters on `stream` (cudaMemsetAsync)
+ *   - Each call clears the array's error word on `stream` (cudaMemsetAsync)
  *     before decoding; the array keeps the rest of the last call's contents.
  *   - All calls on a device share the one array: calls that overlap on the
  *     GPU (for example on two streams) race and give undefined results, so

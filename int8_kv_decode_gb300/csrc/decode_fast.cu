@@ -1,41 +1,52 @@
 // Fast decode over the int8 KV cache: split-KV on tensor cores, fixed-order merge.
 //
-// Work decomposition (all positions absolute within the sequence, fixed at
-// compile time):
-//   * keys are cut into spans of kSpanC = 128; one warp reduces one span with
-//     its own running max, kBlockBk = 16 keys at a time ("在 agent 时代如何快速
-//     验证 kernel 对精度的影响", section "注意力权重": blockwise online softmax,
-//     P rounded only where it multiplies V, row sum from the unrounded P);
-//   * a CTA (grid (nsplit, Hkv, B)) owns a window of 4 consecutive spans of
-//     one (sequence, kv head) for all R = g*M query rows that read that kv
-//     head -- the GQA group times the M draft columns -- so every K/V byte is
-//     read from HBM once; its 4 warps merge their spans at the end;
-//   * the last CTA of a (sequence, kv head) -- found with an acq_rel ticket,
-//     nothing ever waits for another CTA -- merges the windows in order and
-//     divides by the row sum.
+// Three launches on the caller's stream, chained by programmatic dependent
+// launch (a kernel starts while the previous one drains and waits on
+// griddepcontrol before it reads that one's results):
+//   1. prepare_kernel quantizes every query row once (int8 per row) into the
+//      workspace and lists the work items of the valid sequences, one per
+//      window of kSplitC = 512 keys; the rows of an invalid sequence become
+//      NaN and raise an error bit;
+//   2. decode_fast_kernel: persistent CTAs (SM count x occupancy) take the
+//      items x kv heads in a fixed stride.  In a CTA, warp kw reduces span kw
+//      (kSpanC = 128 keys) of the window for all R = g*M query rows that read
+//      the kv head -- the GQA group times the M draft columns -- so every K/V
+//      byte is read from HBM once.  The four spans are merged in a fixed
+//      pairwise order; a sequence of one window is finished here, otherwise
+//      the window's (m, l, o) goes to the workspace;
+//   3. merge_windows_kernel combines the windows of each row in order.
 //
-// Per warp and block of 16 keys:
+// Per warp and block of kBlockBk = 32 keys ("在 agent 时代如何快速验证 kernel
+// 对精度的影响", section "注意力权重": blockwise online softmax, P rounded only
+// where it multiplies V, row sum from the unrounded P):
 //   * TMA (cp.async.bulk.tensor, 128-byte swizzle) streams the K and V rows of
 //     the block into the warp's own ring of shared-memory stages; lane 0 is
-//     the producer, one mbarrier per stage, every wait bounded;
-//   * QK on tensor cores: mma.sync m16n8k16 f16 with f32 accumulation over the
-//     int8 values (exact in f16); every partial sum is an integer below 2^24,
-//     so the f32 scores equal the int32 dot products exactly.  Keys sit on the
-//     MMA's M side, query rows on N (8 per n-tile);
+//     the producer, one mbarrier per stage, every wait bounded.  The producer
+//     runs ahead into the CTA's next work item, so HBM reads go on through
+//     the merge of one window and the start of the next;
+//   * QK on tensor cores: the int8 MMA (m16n8k32) when a warp holds one tile
+//     of 8 query rows, else the f16 MMA (m16n8k16) over exactly converted
+//     values; every partial sum is an integer below 2^24, so the f32 scores
+//     equal the int32 dot products exactly.  Keys sit on the MMA's M side,
+//     query rows on N (8 per n-tile);
 //   * scores, the block max (warp shuffles), the online update of m and l, P
 //     rounding and a = round_p(p) * v_scale in f32 registers;
-//   * PV on tensor cores: mma.sync m16n8k8 tf32 with V (int8, exact in tf32)
-//     on the A side and a split into tf32 hi + lo on the B side, accumulated
-//     in f32; the split keeps float32-level accuracy with no data-dependent
-//     scaling.
+//   * PV on tensor cores: mma.sync m16n8k16 f16 with V (int8, exact in f16)
+//     on the A side and a = round_p(p) * v_scale split into f16 hi + lo on
+//     the B side, accumulated in f32.  a is first scaled by a power of two
+//     fixed per span and row (from the largest v_scale the row sees there),
+//     so the split keeps float32-level accuracy; the power is undone,
+//     exactly, in the merge.
 //
 // Batch invariance ("Kestrel_VLLM - 18" §二): the bytes of a query row depend
 // only on its own keys: spans, blocks and windows sit at fixed key positions,
 // a block with no visible key leaves a row untouched, each MMA output element
 // depends only on its own row's operands, and every merge runs in a fixed
-// order that does not depend on R, M, B or the grid.
+// order that does not depend on R, M, B, the grid or the work schedule.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <atomic>
 
 #include "device_common.cuh"
 
@@ -43,7 +54,7 @@ namespace kattn {
 namespace {
 
 #ifndef KATTN_STAGES
-#define KATTN_STAGES 3
+#define KATTN_STAGES 2
 #endif
 constexpr int kRing = KATTN_STAGES;            // TMA stages per warp
 constexpr int kBlockBytes = kBlockBk * kD;     // one K (or V) block: 4 KB
@@ -55,16 +66,26 @@ struct TmaMaps {
   CUtensorMap k, v;
 };
 
+
+// QK on the int8 MMA when a warp holds one n-tile of query rows (see the kernel).
+#ifndef KATTN_QK_INT8
+#define KATTN_QK_INT8 1
+#endif
+
 template <int NR, int NG>
 struct __align__(1024) SmemT {
-  uint8_t ring[NG * kSpansPerCta][kRing][2][kBlockBytes];  // per warp: [stage][K|V]
+  static constexpr int kRows = NG * NR * 8;                  // query rows of the CTA (rpad)
+  static constexpr int kF = (KATTN_QK_INT8 && NR == 1) ? 1 : 0;   // no f16 fragments
+
+  uint8_t ring[NG * kSpansPerCta][kRing][2][kBlockBytes];    // per warp: [stage][K|V]
+  float slot[NG][2][NR * 8 * kD];                            // span merge, fragment order
+  uint8_t qbuf[kRows * (kD + 4)];                            // item's int8 rows, then scales
+  uint2 qfrag[kF ? 1 : NG][kF ? 1 : NR][kF ? 1 : 8][kF ? 1 : 32];   // f16 query fragments
   uint64_t full[NG * kSpansPerCta][kRing];
-  uint2 qfrag[NG][NR][8][32];                   // query f16 B fragments in lane order
-  int8_t q8[NG * NR * 8][kD];                   // quantized query rows
-  float qs[NG * NR * 8];
-  float wm[NG][kSpansPerCta][NR * 8];           // per-span running max
-  float wl[NG][kSpansPerCta][NR * 8];           // per-span row sum
-  int fail[NG * kSpansPerCta];                  // per warp: a block never arrived
+  uint64_t qbar;
+  float wm[NG][kSpansPerCta][NR * 8];                        // per-span running max
+  float wl[NG][kSpansPerCta][NR * 8];                        // per-span row sum
+  int fail[NG * kSpansPerCta];                               // per warp: a copy never arrived
 };
 
 // ------------------------------------------------------------- PTX helpers
@@ -118,34 +139,12 @@ __device__ __forceinline__ uint32_t i8pair_to_h2(uint32_t xored, uint32_t sel) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// Byte i of a word already XORed with 0x80808080 -> exact float32 of the int8
-// value: the byte becomes the low mantissa of 2^23, then 2^23 + 128 is subtracted.
-__device__ __forceinline__ float i8_to_f32(uint32_t xored, int i) {
-  const uint32_t f = __byte_perm(xored, 0x4B000000u, 0x7540u | (uint32_t)i);
-  return __fsub_rn(__uint_as_float(f), 8388736.0f);
-}
-
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
-  return r;
-}
-
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint2 b) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
       " {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b.x), "r"(b.y));
-}
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
-      " {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void mma_i8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -179,14 +178,14 @@ __device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
   return f2_unpack(r);
 }
 
-// Bytes i and i+1 of a word already XORed with 0x80808080 -> the exact
-// float32 values of the two int8 values (bit patterns), one paired subtract.
-__device__ __forceinline__ uint2 i8pair_to_f32pair(uint32_t xored, int i) {
-  const uint32_t f0 = __byte_perm(xored, 0x4B000000u, 0x7540u | (uint32_t)i);
-  const uint32_t f1 = __byte_perm(xored, 0x4B000000u, 0x7540u | (uint32_t)(i + 1));
-  const float2 v = f2_sub(make_float2(__uint_as_float(f0), __uint_as_float(f1)),
-                          make_float2(8388736.0f, 8388736.0f));   // 2^23 + 128
-  return make_uint2(__float_as_uint(v.x), __float_as_uint(v.y));
+// x = hi + lo with hi = RN_f16(x) and lo = RN_f16(x - hi) (x - hi is exact in
+// float32): 22 significant bits of each of two values, packed as f16x2.
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 r = f2_sub(make_float2(x0, x1), __half22float2(h));
+  const __half2 l = __floats2half2_rn(r.x, r.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // 2^x by the SFU (ex2.approx; subnormal results kept, 2^-inf = +0).
@@ -226,454 +225,686 @@ __device__ __forceinline__ int swz(int row, int chunk) {
   return row * kD + ((chunk ^ (row & 7)) << 4);
 }
 
-// ------------------------------------------------------------------ kernel
+// Programmatic dependent launch: wait until the preceding grid has finished
+// and its writes are visible / let the next grid begin its launch.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Plain bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Named barriers of a warp group (ids 1.. ; 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ------------------------------------------------------------ work items
+// Work item t of the decode grid: window items[t / Hkv] of a sequence, kv
+// head t % Hkv.  b < 0 marks "no item".
+struct Item {
+  int b, w, rs, ctx, kh;
+};
+
+__device__ __forceinline__ Item load_item(const DecodeParams& p, int t, int total) {
+  Item it{-1, 0, 0, 0, 0};
+  if (t < total) {
+    const int4 v = __ldcg(p.items + t / p.Hkv);
+    it = Item{v.x, v.y, v.z, v.w, t % p.Hkv};
+  }
+  return it;
+}
+
+// Keys [s0, s1) of span kw of the item's window, its nb blocks, and the cache
+// row of key s0 in the 2-D view [Hkv * cap_rows][128].
+struct Span {
+  int s0, s1, nb, row;
+};
+
+__device__ __forceinline__ Span span_of(const Item& it, int kw, int M, int cap_rows) {
+  Span s;
+  const int Lmax = it.ctx + M - 1;
+  const int k0 = it.w * kSplitC, k1 = min(k0 + kSplitC, Lmax);
+  s.s0 = k0 + kw * kSpanC;
+  s.s1 = min(s.s0 + kSpanC, k1);
+  s.nb = s.s1 > s.s0 ? (s.s1 - s.s0 + kBlockBk - 1) / kBlockBk : 0;
+  s.row = it.kh * cap_rows + it.rs + s.s0;
+  return s;
+}
+
+// Scales of a span: lane l holds keys l, l+32, l+64, l+96 (0 past the span).
+__device__ __forceinline__ void load_span_scales(const DecodeParams& p, const Item& it,
+                                                 const Span& sp, int lane, float (&ks)[4],
+                                                 float (&vs)[4]) {
+  const int64_t base = (int64_t)it.kh * p.cap_rows + it.rs;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int key = sp.s0 + lane + 32 * e;
+    const bool in = it.b >= 0 && key < sp.s1;
+    ks[e] = in ? __ldg(p.k_scale + base + key) : 0.0f;
+    vs[e] = in ? __ldg(p.v_scale + base + key) : 0.0f;
+  }
+}
+
+// ------------------------------------------------------------------ prepare
+// Blocks [0, q_blocks): one warp per packed query row (b, kv head, r < rpad):
+// row r < R is query (column j = r / g, head kh * g + r % g) quantized per
+// row, rows r >= R are zero.  The last block lists the work items.
+constexpr int kPrepWarps = 4;
+
+__global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodeParams p,
+                                                                  int q_blocks) {
+  griddep_launch_dependents();                    // the decode grid may start its set-up
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if ((int)blockIdx.x < q_blocks) {
+    const int64_t idx = (int64_t)blockIdx.x * kPrepWarps + warp;
+    if (idx >= (int64_t)p.B * p.Hkv * p.rpad) return;
+    const int r = (int)(idx % p.rpad);
+    const int64_t bk = idx / p.rpad;
+    const int kh = (int)(bk % p.Hkv), b = (int)(bk / p.Hkv);
+    uint8_t* pack = p.qpack + bk * qpack_bytes(p.rpad);
+    uint32_t w = 0;
+    float s = 0.0f;
+    if (r < p.R) {
+      const int j = r / p.g, h = kh * p.g + r % p.g;
+      const int64_t orow = (((int64_t)b * p.M + j) * p.Hq + h) * kD;
+      if (sequence_ok(p.row_start[b], p.ctx_len[b], p.M, p.cap_rows, p.max_ctx)) {
+        w = warp_quantize_row(p.q + orow, &s);
+      } else {
+        const float nan = __int_as_float(0x7fc00000);
+        reinterpret_cast<float4*>(p.out + orow)[lane] = make_float4(nan, nan, nan, nan);
+        if (r == 0 && kh == 0 && lane == 0) atomicOr(p.err_word, KATTN_DEVERR_BAD_SEQUENCE);
+      }
+    }
+    reinterpret_cast<uint32_t*>(pack + r * kD)[lane] = w;
+    if (lane == 0) reinterpret_cast<float*>(pack + p.rpad * kD)[r] = s;
+    return;
+  }
+  // The work list: sequences in order, windows in order.
+  __shared__ int warp_total[kPrepWarps];
+  int base = 0;
+  for (int b0 = 0; b0 < p.B; b0 += kPrepWarps * 32) {
+    const int b = b0 + tid;
+    int nw = 0, rs = 0, ctx = 0;
+    if (b < p.B) {
+      const int64_t rs64 = p.row_start[b];
+      ctx = p.ctx_len[b];
+      if (sequence_ok(rs64, ctx, p.M, p.cap_rows, p.max_ctx)) {
+        nw = nsplit_for(ctx + p.M - 1);
+        rs = (int)rs64;                            // < cap_rows: fits
+      }
+    }
+    int incl = nw;                                 // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_total[warp] = incl;
+    __syncthreads();
+    int off = base + incl - nw, chunk = 0;
+#pragma unroll
+    for (int w = 0; w < kPrepWarps; ++w) {
+      if (w < warp) off += warp_total[w];
+      chunk += warp_total[w];
+    }
+    __syncthreads();
+    for (int w = 0; w < nw; ++w) p.items[off + w] = make_int4(b, w, rs, ctx);
+    base += chunk;
+  }
+  if (tid == 0) *p.item_count = (uint32_t)base;
+}
+
+// ------------------------------------------------------------------ decode
 // NR: 8-row n-tiles per warp group; NG: warp groups of kSpansPerCta warps;
-// PM: the P rounding (a kattn_p_mode).  Warp kw of a group reduces span kw of
-// the window for the group's rows, one block of kBlockBk = 32 keys at a time
-// (two MMA halves of 16 keys).
+// PM: the P rounding (a kattn_p_mode).  Warp kw of a group reduces span kw
+// of the item's window for the group's rows, one block of kBlockBk = 32 keys
+// at a time (two MMA halves of 16 keys).
 //
 // QK runs on the int8 MMA (raw K words straight from shared memory, no
 // conversion) when a warp holds a single n-tile of query rows; with more
 // n-tiles the slow int8 tensor rate would bind, so the f16 MMA on converted
 // values is used.  Both give the same exact integer scores.
-#ifndef KATTN_QK_INT8
-#define KATTN_QK_INT8 1
-#endif
 template <int NR, int NG, int PM>
-__global__ void __launch_bounds__(kSpansPerCta * 32 * NG)
+__global__ void __launch_bounds__(kSpansPerCta * 32 * NG, NR == 1 ? 3 : (NG == 1 ? 2 : 1))
 decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   using Smem = SmemT<NR, NG>;
   constexpr bool kQK8 = KATTN_QK_INT8 && NR == 1;
+  constexpr int RG = NR * 8;                      // rows per warp group
+  constexpr int RP = Smem::kRows;                 // rows per CTA (the packed query rows)
+  constexpr int kWarps = kSpansPerCta * NG;
+  constexpr uint32_t kQBytes = RP * (kD + 4);
   extern __shared__ unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  constexpr int RG = NR * 8;                     // rows per warp group
-  constexpr int kWarps = kSpansPerCta * NG;
-  constexpr int kThreads = kWarps * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int kw = warp % kSpansPerCta, grp = warp / kSpansPerCta;
   const int g = lane >> 2, c = lane & 3;
-  const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
-  const int R = p.R, gq = p.g;
+  const int gq = p.g, M = p.M, R = p.R;
   const int row0 = grp * RG;
-
-  const int64_t rs = p.row_start[b];
-  const int ctx = p.ctx_len[b];
-  if (!sequence_ok(rs, ctx, p.M, p.cap_rows, p.max_ctx)) {
-    if (split == 0) {
-      for (int i = tid; i < R * kD; i += kThreads) {
-        const int r = i / kD, j = r / gq, h = kh * gq + r % gq;
-        p.out[(((int64_t)b * p.M + j) * p.Hq + h) * kD + i % kD] = __int_as_float(0x7fc00000);
-      }
-      if (tid == 0 && kh == 0) atomicOr(p.err_word, KATTN_DEVERR_BAD_SEQUENCE);
-    }
-    return;
-  }
-  const int Lmax = ctx + p.M - 1;
-  const int nsplit = nsplit_for(Lmax);
-  if (split >= nsplit) return;
-  const int k0 = split * kSplitC;
-  const int k1 = min(k0 + kSplitC, Lmax);
-  // this warp's span [s0, s1) and its blocks
-  const int s0 = k0 + kw * kSpanC;
-  const int s1 = min(s0 + kSpanC, k1);
-  const int nb = s1 > s0 ? (s1 - s0 + kBlockBk - 1) / kBlockBk : 0;
-  const int tma_row0 = (int)((int64_t)kh * p.cap_rows + rs + s0);
   uint64_t* full = sm.full[warp];
 
-  // ---- per-warp barriers and the first TMA loads (lane 0 is the producer)
-  int issued = 0;                                 // meaningful in lane 0 only
   if (lane == 0) {
     for (int s = 0; s < kRing; ++s) mbar_init(&full[s], 1);
+    if (warp == 0) mbar_init(&sm.qbar, 1);
+    sm.fail[warp] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    for (int s = 0; s < kRing && s < nb; ++s) {
-      mbar_expect_tx(&full[s], 2 * kBlockBytes);
-      tma_load_block(sm.ring[warp][s][0], &maps.k, tma_row0 + s * kBlockBk, &full[s]);
-      tma_load_block(sm.ring[warp][s][1], &maps.v, tma_row0 + s * kBlockBk, &full[s]);
-      ++issued;
-    }
   }
+  __syncthreads();
+  griddep_wait();                                 // the work list and the packed queries
+  griddep_launch_dependents();
 
-  // Scales of this warp's span: lane l holds keys l, l+32, l+64, l+96 (one
-  // load each, issued now so they land while the first blocks stream in).
-  const float* ksb = p.k_scale + (int64_t)kh * p.cap_rows + rs;
-  const float* vsb = p.v_scale + (int64_t)kh * p.cap_rows + rs;
-  float ksp[4], vsp[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int key = s0 + lane + 32 * e;
-    ksp[e] = key < s1 ? __ldg(ksb + key) : 0.0f;
-    vsp[e] = key < s1 ? __ldg(vsb + key) : 0.0f;
-  }
+  const int total = (int)__ldcg(p.item_count) * p.Hkv;
+  const int G = gridDim.x;
+  int t = blockIdx.x;
+  if (t >= total) return;
+  Item it0 = load_item(p, t, total), it1 = load_item(p, t + G, total),
+       it2 = load_item(p, t + 2 * G, total);
 
-  // ---- queries, quantized once per CTA: warp w takes rows w, w + kWarps, ...
-  // (lane l: channels 4l .. 4l+3); bytes and scales go to shared memory.
-  for (int r = warp; r < NG * RG; r += kWarps) {
-    uint32_t w = 0;
-    float qsc = 0.0f;
-    if (r < R) {
-      const int j = r / gq, h = kh * gq + r % gq;
-      w = warp_quantize_row(p.q + (((int64_t)b * p.M + j) * p.Hq + h) * kD, &qsc);
-    }
-    reinterpret_cast<uint32_t*>(sm.q8[r])[lane] = w;
-    if (lane == 0) sm.qs[r] = qsc;
-  }
-  __syncthreads();                                // query bytes and every warp's mbarriers ready
+  bool q_pending = false;                         // thread 0: a query copy in flight
+  auto fetch_queries = [&](const Item& it) {      // thread 0
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    mbar_expect_tx(&sm.qbar, kQBytes);
+    bulk_load(sm.qbuf, p.qpack + ((size_t)it.b * p.Hkv + it.kh) * kQBytes, kQBytes, &sm.qbar);
+    q_pending = true;
+  };
+  if (tid == 0) fetch_queries(it0);
 
-  // Thread (g, c) takes bytes [32c, 32c + 32) of row 8nr + g.  For the int8
-  // MMA, step s covers d = 32c + 8s + 0..7 (words 2s, 2s + 1); for the f16
-  // MMA, step s maps k = 2c,2c+1 -> d = 32c+4s+{0,1} and 2c+8,2c+9 ->
-  // 32c+4s+{2,3}.  Either is a fixed permutation of d shared with the K
-  // fragments, and the sums are integers, so both are exact.
-  uint32_t qw8[8];
-  if constexpr (kQK8) {
-    const uint4* src = reinterpret_cast<const uint4*>(&sm.q8[row0 + g][32 * c]);
-    const uint4 lo = src[0], hi = src[1];
-    qw8[0] = lo.x; qw8[1] = lo.y; qw8[2] = lo.z; qw8[3] = lo.w;
-    qw8[4] = hi.x; qw8[5] = hi.y; qw8[6] = hi.z; qw8[7] = hi.w;
-  } else {
-    if (kw < NR) {                                // warp kw builds n-tile kw of its group
-      const uint4* src = reinterpret_cast<const uint4*>(&sm.q8[row0 + kw * 8 + g][32 * c]);
-      const uint4 lo = src[0], hi = src[1];
-      const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t w = wv[s] ^ 0x80808080u;
-        sm.qfrag[grp][kw][s][lane] = make_uint2(i8pair_to_h2(w, 0x4140u), i8pair_to_h2(w, 0x4342u));
-      }
-    }
-    __syncthreads();
-  }
-  float qs_row[NR][2];                            // scales of rows 8nr + 2c + e
-#pragma unroll
-  for (int nr = 0; nr < NR; ++nr)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) qs_row[nr][e] = sm.qs[row0 + nr * 8 + 2 * c + e];
-
-  // ---- per-thread row state: rows 8nr + 2c + e (e = 0, 1) of the group
-  float m_run[NR][2], l_run[NR][2];
-  int Lrow[NR][2];
-#pragma unroll
-  for (int nr = 0; nr < NR; ++nr)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      m_run[nr][e] = -INFINITY;
-      l_run[nr][e] = 0.0f;
-      Lrow[nr][e] = ctx + (row0 + nr * 8 + 2 * c + e) / gq;
-    }
-  float o[8][NR][4];
-#pragma unroll
-  for (int md = 0; md < 8; ++md)
-#pragma unroll
-    for (int nr = 0; nr < NR; ++nr)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) o[md][nr][u] = 0.0f;
-
-  int fail_blk = -1;
-  int st = 0;                                     // ring stage of block i
-  uint32_t ph = 0;                                // its mbarrier phase parity
-  for (int i = 0; i < nb; ++i) {
-    const int t0 = s0 + i * kBlockBk;
-    // scales of keys 32i + g + 8q (q = 0..3): lane g + 8q, register i
-    float ks4[4], vs4[4];
-    {
-      const float kse = i == 0 ? ksp[0] : i == 1 ? ksp[1] : i == 2 ? ksp[2] : ksp[3];
-      const float vse = i == 0 ? vsp[0] : i == 1 ? vsp[1] : i == 2 ? vsp[2] : vsp[3];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        ks4[q] = __shfl_sync(0xffffffffu, kse, g + 8 * q);
-        vs4[q] = __shfl_sync(0xffffffffu, vse, g + 8 * q);
-      }
-    }
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[st], ph))) {
-      fail_blk = i;
-      break;
-    }
-    const uint8_t* Kt = sm.ring[warp][st][0];
-    const uint8_t* Vt = sm.ring[warp][st][1];
-
-    // ---- QK for both 16-key halves hf.  sc[hf][nr]: [0] key 16hf+g row 2c,
-    // [1] key 16hf+g row 2c+1, [2] key 16hf+g+8 row 2c, [3] key 16hf+g+8 row
-    // 2c+1 (rows inside n-tile nr).
-    float sc[2][NR][4];
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int ra = 16 * hf + g, rb = ra + 8;
-      const uint4 a_lo = lds128(Kt + swz(ra, 2 * c)), a_hi = lds128(Kt + swz(ra, 2 * c + 1));
-      const uint4 b_lo = lds128(Kt + swz(rb, 2 * c)), b_hi = lds128(Kt + swz(rb, 2 * c + 1));
-      const uint32_t wa[8] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w, a_hi.x, a_hi.y, a_hi.z, a_hi.w};
-      const uint32_t wb[8] = {b_lo.x, b_lo.y, b_lo.z, b_lo.w, b_hi.x, b_hi.y, b_hi.z, b_hi.w};
-      if constexpr (kQK8) {
-        int iacc[4] = {0, 0, 0, 0}, iacc2[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          mma_i8((s & 1) ? iacc2 : iacc, wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1],
-                 qw8[2 * s], qw8[2 * s + 1]);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sc[hf][0][u] = __int2float_rn(iacc[u] + iacc2[u]);
+  // ---- producer: lane 0 issues, every lane keeps the same counters.  The
+  // cursor runs over this item's blocks, then the next item's.
+  Span psp = span_of(it0, kw, M, p.cap_rows);
+  int pitem = 0, pblk = 0, ist = 0, inflight = 0;
+  auto produce = [&]() {
+    while (inflight < kRing) {
+      if (pblk < psp.nb) {
+        if (lane == 0) {
+          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+          mbar_expect_tx(&full[ist], 2 * kBlockBytes);
+          const int row = psp.row + pblk * kBlockBk;
+          tma_load_block(sm.ring[warp][ist][0], &maps.k, row, &full[ist]);
+          tma_load_block(sm.ring[warp][ist][1], &maps.v, row, &full[ist]);
+        }
+        ++pblk;
+        ++inflight;
+        ist = ist + 1 == kRing ? 0 : ist + 1;
+      } else if (pitem == 0 && it1.b >= 0) {
+        pitem = 1;
+        pblk = 0;
+        psp = span_of(it1, kw, M, p.cap_rows);
       } else {
-        float sacc[NR][4], sacc2[NR][4];
-#pragma unroll
-        for (int nr = 0; nr < NR; ++nr)
-#pragma unroll
-          for (int u = 0; u < 4; ++u) sacc[nr][u] = sacc2[nr][u] = 0.0f;
+        break;
+      }
+    }
+  };
+  produce();
+
+  // ---- consumer state
+  Span sp = span_of(it0, kw, M, p.cap_rows);
+  float ksp[4], vsp[4], ksn[4], vsn[4];           // this item's / the next item's span scales
+  load_span_scales(p, it0, sp, lane, ksp, vsp);
+  load_span_scales(p, it1, span_of(it1, kw, M, p.cap_rows), lane, ksn, vsn);
+  int cst = 0;                                    // ring stage of the next block to consume
+  uint32_t cph = 0, qph = 0;                      // its mbarrier parity; the query barrier's
+
+  for (;;) {
+    // ---- the item's queries (packed by prepare_kernel)
+    const bool q_ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sm.qbar, qph));
+    if (tid == 0 && q_ok) q_pending = false;
+    // Thread (g, c) takes bytes [32c, 32c + 32) of row 8nr + g.  For the int8
+    // MMA, step s covers d = 32c + 8s + 0..7 (words 2s, 2s + 1); for the f16
+    // MMA, step s maps k = 2c,2c+1 -> d = 32c+4s+{0,1} and 2c+8,2c+9 ->
+    // 32c+4s+{2,3}.  Either is a fixed permutation of d shared with the K
+    // fragments, and the sums are integers, so both are exact.
+    uint32_t qw8[8];
+    if constexpr (kQK8) {
+      const uint4* src = reinterpret_cast<const uint4*>(&sm.qbuf[(row0 + g) * kD + 32 * c]);
+      const uint4 lo = src[0], hi = src[1];
+      qw8[0] = lo.x; qw8[1] = lo.y; qw8[2] = lo.z; qw8[3] = lo.w;
+      qw8[4] = hi.x; qw8[5] = hi.y; qw8[6] = hi.z; qw8[7] = hi.w;
+    } else {
+      if (kw < NR) {                              // warp kw builds n-tile kw of its group
+        const uint4* src =
+            reinterpret_cast<const uint4*>(&sm.qbuf[(row0 + kw * 8 + g) * kD + 32 * c]);
+        const uint4 lo = src[0], hi = src[1];
+        const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t xa = wa[s] ^ 0x80808080u, xb = wb[s] ^ 0x80808080u;
-          const uint32_t af[4] = {i8pair_to_h2(xa, 0x4140u), i8pair_to_h2(xb, 0x4140u),
-                                  i8pair_to_h2(xa, 0x4342u), i8pair_to_h2(xb, 0x4342u)};
-#pragma unroll
-          for (int nr = 0; nr < NR; ++nr)
-            mma_f16((s & 1) ? sacc2[nr] : sacc[nr], af, sm.qfrag[grp][nr][s][lane]);
+          const uint32_t w = wv[s] ^ 0x80808080u;
+          sm.qfrag[grp][kw][s][lane] = make_uint2(i8pair_to_h2(w, 0x4140u), i8pair_to_h2(w, 0x4342u));
         }
-#pragma unroll
-        for (int nr = 0; nr < NR; ++nr)
-#pragma unroll
-          for (int u = 0; u < 4; ++u) sc[hf][nr][u] = __fadd_rn(sacc[nr][u], sacc2[nr][u]);
       }
+      __syncthreads();
     }
-
-    // ---- scores s = ((S * (qs * ks)) * sm_scale), masked past each row's L
-    const bool all_visible = t0 + kBlockBk <= ctx;   // ctx is the smallest L of any row
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf)
+    float qs_row[NR][2];                          // scales of rows 8nr + 2c + e
+    {
+      const float* qsb = reinterpret_cast<const float*>(&sm.qbuf[RP * kD]);
 #pragma unroll
       for (int nr = 0; nr < NR; ++nr)
 #pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {            // k2: key g (0) or g + 8 (1)
-          const float ksv = ks4[2 * hf + k2];
-          const float2 qk = f2_mul(make_float2(qs_row[nr][0], qs_row[nr][1]), make_float2(ksv, ksv));
-          float2 s2 = f2_mul(make_float2(sc[hf][nr][2 * k2], sc[hf][nr][2 * k2 + 1]), qk);
-          s2 = f2_mul(s2, make_float2(p.sm_scale, p.sm_scale));
-          const int key = t0 + 16 * hf + g + 8 * k2;
-          sc[hf][nr][2 * k2] = (all_visible || key < Lrow[nr][0]) ? s2.x : -INFINITY;
-          sc[hf][nr][2 * k2 + 1] = (all_visible || key < Lrow[nr][1]) ? s2.y : -INFINITY;
-        }
+        for (int e = 0; e < 2; ++e) qs_row[nr][e] = qsb[row0 + nr * 8 + 2 * c + e];
+    }
 
-    // ---- online softmax update of rows 8nr + 2c + e over the 32-key block
-    float alpha[NR][2];
-    bool rescale = false;
+    // Power of two 2^E per query row: over the keys of the span that the row
+    // sees, max_k v_scale_k * 2^E lies in [2^14, 2^15), so a = round_p(p) *
+    // v_scale * 2^E stays in the normal f16 range down to weights far below
+    // the ones that matter; the row's o is held in units of 2^E.  E depends
+    // only on the row's own keys (batch invariance).
+    const int ctx = it0.ctx;
+    float up_row[NR][2], down_row[NR][2];
+    {
+      const int kc = min(sp.s1, ctx);             // keys every row sees: [s0, kc)
+      float vm = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (sp.s0 + lane + 32 * e < kc) vm = fmaxf(vm, vsp[e]);
+      vm = warp_max(vm);
+      float vt[kMaxM - 1];                       // scales of keys ctx + t (the draft tail)
+#pragma unroll
+      for (int t = 0; t < kMaxM - 1; ++t) {
+        const int rel = ctx + t - sp.s0;          // uniform over the warp
+        float v = 0.0f;
+        if (t < M - 1 && rel >= 0 && ctx + t < sp.s1) {
+          const int e = rel >> 5;
+          const float mine = e == 0 ? vsp[0] : e == 1 ? vsp[1] : e == 2 ? vsp[2] : vsp[3];
+          v = __shfl_sync(0xffffffffu, mine, rel & 31);
+        }
+        vt[t] = v;
+      }
+#pragma unroll
+      for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int jr = min((row0 + nr * 8 + 2 * c + e) / gq, M - 1);
+          float vmax = vm;
+#pragma unroll
+          for (int t = 0; t < kMaxM - 1; ++t)
+            if (t < jr) vmax = fmaxf(vmax, vt[t]);
+          const int bexp = min(max(268 - (int)((__float_as_uint(vmax) >> 23) & 0xffu), 1), 253);
+          up_row[nr][e] = __uint_as_float((uint32_t)bexp << 23);
+          down_row[nr][e] = __uint_as_float((uint32_t)(254 - bexp) << 23);
+        }
+    }
+
+    // ---- per-thread row state: rows 8nr + 2c + e (e = 0, 1) of the group
+    float m_run[NR][2], l_run[NR][2];
+    int Lrow[NR][2];
 #pragma unroll
     for (int nr = 0; nr < NR; ++nr)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float bm = fmaxf(fmaxf(sc[0][nr][e], sc[0][nr][2 + e]), fmaxf(sc[1][nr][e], sc[1][nr][2 + e]));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-        const float mnew = fmaxf(m_run[nr][e], bm);
-        float a = 1.0f, pk[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
-        if (mnew != -INFINITY) {                  // else: no visible key yet, row untouched
-          a = exp_diff(m_run[nr][e], mnew);
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            pk[hf][0] = exp_diff(sc[hf][nr][e], mnew);
-            pk[hf][1] = exp_diff(sc[hf][nr][2 + e], mnew);
-          }
-        }
-        alpha[nr][e] = a;
-        rescale |= (a != 1.0f);
-        m_run[nr][e] = mnew;
-        l_run[nr][e] = __fmaf_rn(l_run[nr][e], a,
-                                 __fadd_rn(__fadd_rn(pk[0][0], pk[0][1]), __fadd_rn(pk[1][0], pk[1][1])));
-        // a = round_p(p) * v_scale, kept in the score layout (sc is done with)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          sc[hf][nr][e] = __fmul_rn(round_p_t<PM>(pk[hf][0]), vs4[2 * hf]);
-          sc[hf][nr][2 + e] = __fmul_rn(round_p_t<PM>(pk[hf][1]), vs4[2 * hf + 1]);
-        }
+        m_run[nr][e] = -INFINITY;
+        l_run[nr][e] = 0.0f;
+        Lrow[nr][e] = ctx + min((row0 + nr * 8 + 2 * c + e) / gq, M - 1);
       }
-    if (rescale) {
-#pragma unroll
-      for (int md = 0; md < 8; ++md)
-#pragma unroll
-        for (int nr = 0; nr < NR; ++nr) {
-          const float2 a2 = make_float2(alpha[nr][0], alpha[nr][1]);
-          const float2 lo = f2_mul(make_float2(o[md][nr][0], o[md][nr][1]), a2);
-          const float2 hi = f2_mul(make_float2(o[md][nr][2], o[md][nr][3]), a2);
-          o[md][nr][0] = lo.x; o[md][nr][1] = lo.y; o[md][nr][2] = hi.x; o[md][nr][3] = hi.y;
-        }
-    }
-
-    // ---- PV, one 16-key half at a time
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      // B fragments (tf32, query rows on N): for k-step h, b0 = P[key 2c+8h][row g],
-      // b1 = P[key 2c+1+8h][row g].  P[key x][row y] sits in lane
-      // 4 * (x & 7) + (y >> 1), register (x >= 8 ? 2 : 0) + (y & 1) of the
-      // score layout.
-      uint32_t bhi[NR][2][2], blo[NR][2][2];
-      {
-        const int srcA = 8 * c + (g >> 1), srcB = srcA + 4;
-        const bool odd = g & 1;
-#pragma unroll
-        for (int nr = 0; nr < NR; ++nr) {
-          float fA[4], fB[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            fA[u] = __shfl_sync(0xffffffffu, sc[hf][nr][u], srcA);
-            fB[u] = __shfl_sync(0xffffffffu, sc[hf][nr][u], srcB);
-          }
-          const float vv[2][2] = {{odd ? fA[1] : fA[0], odd ? fB[1] : fB[0]},
-                                  {odd ? fA[3] : fA[2], odd ? fB[3] : fB[2]}};
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t h0 = to_tf32(vv[h][0]), h1 = to_tf32(vv[h][1]);
-            const float2 rest = f2_sub(make_float2(vv[h][0], vv[h][1]),
-                                       make_float2(__uint_as_float(h0), __uint_as_float(h1)));
-            bhi[nr][h][0] = h0;
-            bhi[nr][h][1] = h1;
-            blo[nr][h][0] = to_tf32(rest.x);
-            blo[nr][h][1] = to_tf32(rest.y);
-          }
-        }
-      }
-      // A = V^T (MMA rows = channels, cols = keys).  Thread (g, c) reads keys
-      // 2c, 2c+1, 2c+8, 2c+9 of the half and channels 16g .. 16g+15; m-tile
-      // md row g is d = 16g + 2md, row g + 8 is d + 1.
-      const int kr = 16 * hf + 2 * c;
-      const uint4 vw0 = lds128(Vt + swz(kr, g)), vw1 = lds128(Vt + swz(kr + 1, g));
-      const uint4 vw2 = lds128(Vt + swz(kr + 8, g)), vw3 = lds128(Vt + swz(kr + 9, g));
-      const uint32_t x[4][4] = {
-          {vw0.x ^ 0x80808080u, vw0.y ^ 0x80808080u, vw0.z ^ 0x80808080u, vw0.w ^ 0x80808080u},
-          {vw1.x ^ 0x80808080u, vw1.y ^ 0x80808080u, vw1.z ^ 0x80808080u, vw1.w ^ 0x80808080u},
-          {vw2.x ^ 0x80808080u, vw2.y ^ 0x80808080u, vw2.z ^ 0x80808080u, vw2.w ^ 0x80808080u},
-          {vw3.x ^ 0x80808080u, vw3.y ^ 0x80808080u, vw3.z ^ 0x80808080u, vw3.w ^ 0x80808080u}};
-#pragma unroll
-      for (int md = 0; md < 8; ++md) {
-        const int wi = md >> 1, bi = 2 * (md & 1);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint2 p01 = i8pair_to_f32pair(x[2 * h][wi], bi);       // key 2c+8h, d, d+1
-          const uint2 p23 = i8pair_to_f32pair(x[2 * h + 1][wi], bi);   // key 2c+1+8h
-          const uint32_t af[4] = {p01.x, p01.y, p23.x, p23.y};
-#pragma unroll
-          for (int nr = 0; nr < NR; ++nr) {
-            mma_tf32(o[md][nr], af, bhi[nr][h][0], bhi[nr][h][1]);
-            mma_tf32(o[md][nr], af, blo[nr][h][0], blo[nr][h][1]);
-          }
-        }
-      }
-    }
-
-    // ---- refill the stage just read with block i + kRing
-    __syncwarp();
-    if (lane == 0 && i + kRing < nb) {
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      mbar_expect_tx(&full[st], 2 * kBlockBytes);
-      tma_load_block(sm.ring[warp][st][0], &maps.k, tma_row0 + (i + kRing) * kBlockBk, &full[st]);
-      tma_load_block(sm.ring[warp][st][1], &maps.v, tma_row0 + (i + kRing) * kBlockBk, &full[st]);
-      ++issued;
-    }
-    if (++st == kRing) {
-      st = 0;
-      ph ^= 1u;
-    }
-  }
-
-  if (lane == 0) {
-    sm.fail[warp] = fail_blk >= 0;
-    if (fail_blk >= 0) {
-      // A block never arrived: flag it and give the copies still in flight a
-      // bounded chance to land before the CTA leaves.
-      atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
-      for (int i = fail_blk; i < issued; ++i)
-        mbar_wait_bounded(&full[i % kRing], (uint32_t)((i / kRing) & 1));
-    }
-  }
-
-  // ---- per-span row sums and maxima
-#pragma unroll
-  for (int nr = 0; nr < NR; ++nr)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float v = l_run[nr][e];
-      v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 4));
-      v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 8));
-      v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      if (g == 0) {
-        sm.wl[grp][kw][nr * 8 + 2 * c + e] = v;
-        sm.wm[grp][kw][nr * 8 + 2 * c + e] = m_run[nr][e];
-      }
-    }
-  __syncthreads();
-  {
-    int any_fail = 0;                             // uniform: read after the barrier
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) any_fail |= sm.fail[w];
-    if (any_fail) return;
-  }
-
-  // ---- merge the window's 4 spans in span order: each warp writes its o,
-  // weighted by e^(m_span - m_window), to its own slot; one barrier; then
-  // every (row, d) sums the slots in order.  The TMA ring is idle now and
-  // holds the slots: [kSpansPerCta][NG * RG][kD].
-  float* slots = reinterpret_cast<float*>(&sm.ring[0][0][0][0]);
-  constexpr int kSlot = NG * RG * kD;
-  static_assert(sizeof(sm.ring) >= kSpansPerCta * kSlot * sizeof(float),
-                "the idle TMA ring must hold one slot per span");
-#pragma unroll
-  for (int nr = 0; nr < NR; ++nr) {
-    float wt[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int rr = nr * 8 + 2 * c + e;
-      float m = sm.wm[grp][0][rr];
-#pragma unroll
-      for (int w = 1; w < kSpansPerCta; ++w) m = fmaxf(m, sm.wm[grp][w][rr]);
-      wt[e] = merge_weight(sm.wm[grp][kw][rr], m);
-    }
+    float o[8][NR][4];
 #pragma unroll
     for (int md = 0; md < 8; ++md)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int rr = row0 + nr * 8 + 2 * c + (u & 1);
-        slots[kw * kSlot + rr * kD + 16 * g + 2 * md + (u >> 1)] = __fmul_rn(o[md][nr][u], wt[u & 1]);
-      }
-  }
-  __syncthreads();
+      for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) o[md][nr][u] = 0.0f;
 
-  const int64_t out_b = (int64_t)b * p.M;
-  const size_t pstride = (size_t)R * (kD + 2);
-  float* part = p.partials + (((size_t)b * p.nsplit_max + split) * p.Hkv + kh) * pstride;
-  for (int i = tid; i < R * kD; i += kThreads) {
-    const int r = i / kD, gi = r / RG, rr = r % RG;
-    float m = sm.wm[gi][0][rr];
+    bool failed = !q_ok;
+    const int nb = q_ok ? sp.nb : 0;
+    for (int i = 0; i < nb; ++i) {
+      const int t0 = sp.s0 + i * kBlockBk;
+      // scales of keys 32i + g + 8q (q = 0..3): lane g + 8q, register i
+      float ks4[4], vs4[4];
+      {
+        const float kse = i == 0 ? ksp[0] : i == 1 ? ksp[1] : i == 2 ? ksp[2] : ksp[3];
+        const float vse = i == 0 ? vsp[0] : i == 1 ? vsp[1] : i == 2 ? vsp[2] : vsp[3];
 #pragma unroll
-    for (int w = 1; w < kSpansPerCta; ++w) m = fmaxf(m, sm.wm[gi][w][rr]);
-    float l = 0.0f, ov = 0.0f;
+        for (int q = 0; q < 4; ++q) {
+          ks4[q] = __shfl_sync(0xffffffffu, kse, g + 8 * q);
+          vs4[q] = __shfl_sync(0xffffffffu, vse, g + 8 * q);
+        }
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[cst], cph))) {
+        failed = true;
+        break;
+      }
+      const uint8_t* Kt = sm.ring[warp][cst][0];
+      const uint8_t* Vt = sm.ring[warp][cst][1];
+      // ---- QK for both 16-key halves hf.  sc[hf][nr]: [0] key 16hf+g row 2c,
+      // [1] key 16hf+g row 2c+1, [2] key 16hf+g+8 row 2c, [3] key 16hf+g+8 row
+      // 2c+1 (rows inside n-tile nr).
+      float sc[2][NR][4];
 #pragma unroll
-    for (int w = 0; w < kSpansPerCta; ++w) {
-      l = __fmaf_rn(sm.wl[gi][w][rr], merge_weight(sm.wm[gi][w][rr], m), l);
-      ov = (w == 0) ? slots[i] : __fadd_rn(ov, slots[w * kSlot + i]);
+      for (int hf = 0; hf < 2; ++hf) {
+        const int ra = 16 * hf + g, rb = ra + 8;
+        const uint4 a_lo = lds128(Kt + swz(ra, 2 * c)), a_hi = lds128(Kt + swz(ra, 2 * c + 1));
+        const uint4 b_lo = lds128(Kt + swz(rb, 2 * c)), b_hi = lds128(Kt + swz(rb, 2 * c + 1));
+        const uint32_t wa[8] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w, a_hi.x, a_hi.y, a_hi.z, a_hi.w};
+        const uint32_t wb[8] = {b_lo.x, b_lo.y, b_lo.z, b_lo.w, b_hi.x, b_hi.y, b_hi.z, b_hi.w};
+        if constexpr (kQK8) {
+          int iacc[4] = {0, 0, 0, 0}, iacc2[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            mma_i8((s & 1) ? iacc2 : iacc, wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1],
+                   qw8[2 * s], qw8[2 * s + 1]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) sc[hf][0][u] = __int2float_rn(iacc[u] + iacc2[u]);
+        } else {
+          float sacc[NR][4], sacc2[NR][4];
+#pragma unroll
+          for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sacc[nr][u] = sacc2[nr][u] = 0.0f;
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const uint32_t xa = wa[s] ^ 0x80808080u, xb = wb[s] ^ 0x80808080u;
+            const uint32_t af[4] = {i8pair_to_h2(xa, 0x4140u), i8pair_to_h2(xb, 0x4140u),
+                                    i8pair_to_h2(xa, 0x4342u), i8pair_to_h2(xb, 0x4342u)};
+#pragma unroll
+            for (int nr = 0; nr < NR; ++nr)
+              mma_f16((s & 1) ? sacc2[nr] : sacc[nr], af, sm.qfrag[grp][nr][s][lane]);
+          }
+#pragma unroll
+          for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sc[hf][nr][u] = __fadd_rn(sacc[nr][u], sacc2[nr][u]);
+        }
+      }
+
+      // ---- scores s = ((S * (qs * ks)) * sm_scale), masked past each row's L
+      const bool all_visible = t0 + kBlockBk <= ctx;   // ctx is the smallest L of any row
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {            // k2: key g (0) or g + 8 (1)
+            const float ksv = ks4[2 * hf + k2];
+            const float2 qk = f2_mul(make_float2(qs_row[nr][0], qs_row[nr][1]), make_float2(ksv, ksv));
+            float2 s2 = f2_mul(make_float2(sc[hf][nr][2 * k2], sc[hf][nr][2 * k2 + 1]), qk);
+            s2 = f2_mul(s2, make_float2(p.sm_scale, p.sm_scale));
+            const int key = t0 + 16 * hf + g + 8 * k2;
+            sc[hf][nr][2 * k2] = (all_visible || key < Lrow[nr][0]) ? s2.x : -INFINITY;
+            sc[hf][nr][2 * k2 + 1] = (all_visible || key < Lrow[nr][1]) ? s2.y : -INFINITY;
+          }
+
+      // ---- online softmax update of rows 8nr + 2c + e over the 32-key block
+      float alpha[NR][2];
+      bool rescale = false;
+#pragma unroll
+      for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float bm = fmaxf(fmaxf(sc[0][nr][e], sc[0][nr][2 + e]), fmaxf(sc[1][nr][e], sc[1][nr][2 + e]));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+          const float mnew = fmaxf(m_run[nr][e], bm);
+          float a = 1.0f, pk[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+          if (mnew != -INFINITY) {                  // else: no visible key yet, row untouched
+            a = exp_diff(m_run[nr][e], mnew);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              pk[hf][0] = exp_diff(sc[hf][nr][e], mnew);
+              pk[hf][1] = exp_diff(sc[hf][nr][2 + e], mnew);
+            }
+          }
+          alpha[nr][e] = a;
+          rescale |= (a != 1.0f);
+          m_run[nr][e] = mnew;
+          l_run[nr][e] = __fmaf_rn(l_run[nr][e], a,
+                                   __fadd_rn(__fadd_rn(pk[0][0], pk[0][1]), __fadd_rn(pk[1][0], pk[1][1])));
+          // a = round_p(p) * v_scale, kept in the score layout (sc is done with)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            sc[hf][nr][e] = __fmul_rn(__fmul_rn(round_p_t<PM>(pk[hf][0]), vs4[2 * hf]), up_row[nr][e]);
+            sc[hf][nr][2 + e] =
+                __fmul_rn(__fmul_rn(round_p_t<PM>(pk[hf][1]), vs4[2 * hf + 1]), up_row[nr][e]);
+          }
+        }
+      if (rescale) {
+#pragma unroll
+        for (int md = 0; md < 8; ++md)
+#pragma unroll
+          for (int nr = 0; nr < NR; ++nr) {
+            const float2 a2 = make_float2(alpha[nr][0], alpha[nr][1]);
+            const float2 lo = f2_mul(make_float2(o[md][nr][0], o[md][nr][1]), a2);
+            const float2 hi = f2_mul(make_float2(o[md][nr][2], o[md][nr][3]), a2);
+            o[md][nr][0] = lo.x; o[md][nr][1] = lo.y; o[md][nr][2] = hi.x; o[md][nr][3] = hi.y;
+          }
+      }
+
+      // ---- PV, one 16-key half at a time, on the f16 MMA (m16n8k16)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        // B fragments (query rows on N): b0 = {a[key 2c][row g], a[key 2c+1][row g]},
+        // b1 = {a[key 2c+8][row g], a[key 2c+9][row g]} (keys of the half), each
+        // split into f16 hi + lo.  a[key x][row y] sits in lane
+        // 4 * (x & 7) + (y >> 1), register (x >= 8 ? 2 : 0) + (y & 1) of the
+        // score layout.
+        uint2 bhi[NR], blo[NR];
+        {
+          const int srcA = 8 * c + (g >> 1), srcB = srcA + 4;
+          const bool odd = g & 1;
+#pragma unroll
+          for (int nr = 0; nr < NR; ++nr) {
+            float fA[4], fB[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              fA[u] = __shfl_sync(0xffffffffu, sc[hf][nr][u], srcA);
+              fB[u] = __shfl_sync(0xffffffffu, sc[hf][nr][u], srcB);
+            }
+            split_f16x2(odd ? fA[1] : fA[0], odd ? fB[1] : fB[0], bhi[nr].x, blo[nr].x);
+            split_f16x2(odd ? fA[3] : fA[2], odd ? fB[3] : fB[2], bhi[nr].y, blo[nr].y);
+          }
+        }
+        // A = V^T (MMA rows = channels, cols = keys).  Thread (g, c) reads keys
+        // 2c, 2c+1, 2c+8, 2c+9 of the half and channels 16g .. 16g+15; m-tile
+        // md row g is d = 16g + 2md, row g + 8 is d + 1.  One byte permute
+        // pairs the two keys of a channel, a second places each byte (XOR 0x80)
+        // in the mantissa of 1024, and 1152 is subtracted: exact f16 values.
+        const int kr = 16 * hf + 2 * c;
+        const uint4 vw0 = lds128(Vt + swz(kr, g)), vw1 = lds128(Vt + swz(kr + 1, g));
+        const uint4 vw2 = lds128(Vt + swz(kr + 8, g)), vw3 = lds128(Vt + swz(kr + 9, g));
+        const uint32_t w0[4] = {vw0.x, vw0.y, vw0.z, vw0.w}, w1[4] = {vw1.x, vw1.y, vw1.z, vw1.w};
+        const uint32_t w2[4] = {vw2.x, vw2.y, vw2.z, vw2.w}, w3[4] = {vw3.x, vw3.y, vw3.z, vw3.w};
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          const int wi = md >> 1;
+          const uint32_t sel = (md & 1) ? 0x7362u : 0x5140u;   // bytes j, j+1 of both words
+          const uint32_t t01 = __byte_perm(w0[wi], w1[wi], sel) ^ 0x80808080u;
+          const uint32_t t23 = __byte_perm(w2[wi], w3[wi], sel) ^ 0x80808080u;
+          const uint32_t af[4] = {i8pair_to_h2(t01, 0x4140u), i8pair_to_h2(t01, 0x4342u),
+                                  i8pair_to_h2(t23, 0x4140u), i8pair_to_h2(t23, 0x4342u)};
+#pragma unroll
+          for (int nr = 0; nr < NR; ++nr) {
+            mma_f16(o[md][nr], af, bhi[nr]);
+            mma_f16(o[md][nr], af, blo[nr]);
+          }
+        }
+      }
+
+      __syncwarp();
+      --inflight;
+      if (++cst == kRing) {
+        cst = 0;
+        cph ^= 1u;
+      }
+      produce();                                  // refill the stage just read
     }
-    if (nsplit == 1) {                            // the whole sequence: final output
-      const int j = r / gq, h = kh * gq + r % gq;
-      p.out[((out_b + j) * p.Hq + h) * kD + i % kD] = __fdiv_rn(ov, l);
-    } else {                                      // this window's partial (m, l, o)
-      part[i] = ov;
-      if (i % kD == 0) {
-        part[(size_t)R * kD + r] = m;
-        part[(size_t)R * kD + R + r] = l;
+
+    // ---- per-span row sums and maxima
+#pragma unroll
+    for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = l_run[nr][e];
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        if (g == 0) {
+          sm.wl[grp][kw][nr * 8 + 2 * c + e] = v;
+          sm.wm[grp][kw][nr * 8 + 2 * c + e] = m_run[nr][e];
+        }
+      }
+    if (lane == 0 && failed) sm.fail[warp] = 1;
+    __syncthreads();
+    {
+      int any_fail = 0;                           // uniform: read after the barrier
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) any_fail |= sm.fail[w];
+      if (any_fail) {
+        // A copy never arrived: flag it, give every copy still in flight a
+        // bounded chance to land, then leave.
+        if (lane == 0) {
+          if (failed) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
+          int s = cst;
+          uint32_t ph = cph;
+          for (int k = 0; k < inflight; ++k) {
+            mbar_wait_bounded(&full[s], ph);
+            if (++s == kRing) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          if (tid == 0 && q_pending) mbar_wait_bounded(&sm.qbar, qph);
+        }
+        return;
       }
     }
+    // Every warp is done with this item's queries: fetch the next item's.
+    if (tid == 0 && it1.b >= 0) fetch_queries(it1);
+
+    // ---- merge of the window's 4 spans, in the fixed order
+    //   o = (w0 o0 + w1 o1) + (w2 o2 + w3 o3),   w_s = e^(m_s - max_s m_s):
+    // warps 1 and 3 write w o to their slot, warps 0 and 2 add theirs, warp 0
+    // adds warp 2's sum and writes the result.  Slots hold a warp's
+    // accumulator fragments in register order (conflict-free).
+    float wt[NR][2], mwin[NR][2];
+#pragma unroll
+    for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int rr = nr * 8 + 2 * c + e;
+        float m = sm.wm[grp][0][rr];
+#pragma unroll
+        for (int w = 1; w < kSpansPerCta; ++w) m = fmaxf(m, sm.wm[grp][w][rr]);
+        mwin[nr][e] = m;
+        wt[nr][e] = __fmul_rn(merge_weight(sm.wm[grp][kw][rr], m), down_row[nr][e]);
+      }
+    const int bar_pair = 1 + 2 * grp, bar_even = 2 + 2 * grp;
+    float* slot = sm.slot[grp][kw >> 1];
+    if (kw & 1) {
+#pragma unroll
+      for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+        for (int md = 0; md < 8; ++md)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            slot[((nr * 8 + md) * 4 + u) * 32 + lane] = __fmul_rn(o[md][nr][u], wt[nr][u & 1]);
+      named_arrive(bar_pair, kSpansPerCta * 32);
+    } else {
+      named_sync(bar_pair, kSpansPerCta * 32);
+#pragma unroll
+      for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+        for (int md = 0; md < 8; ++md)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float& x = slot[((nr * 8 + md) * 4 + u) * 32 + lane];
+            o[md][nr][u] = __fmaf_rn(o[md][nr][u], wt[nr][u & 1], x);
+            if (kw == 2) x = o[md][nr][u];
+          }
+      named_sync(bar_even, 2 * 32);
+      if (kw == 0) {
+        const float* other = sm.slot[grp][1];
+#pragma unroll
+        for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+          for (int md = 0; md < 8; ++md)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              o[md][nr][u] = __fadd_rn(o[md][nr][u], other[((nr * 8 + md) * 4 + u) * 32 + lane]);
+        const bool whole = nsplit_for(ctx + M - 1) == 1;   // the sequence is one window
+        const int kh = it0.kh, b = it0.b;
+        float* part = p.partials +
+                      (((size_t)b * p.nsplit_max + it0.w) * p.Hkv + kh) * partial_stride(R);
+#pragma unroll
+        for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int rr = nr * 8 + 2 * c + e, r = row0 + rr;
+            if (r >= R) continue;
+            float l = 0.0f;                       // window row sum, spans in order
+#pragma unroll
+            for (int w = 0; w < kSpansPerCta; ++w)
+              l = __fmaf_rn(sm.wl[grp][w][rr], merge_weight(sm.wm[grp][w][rr], mwin[nr][e]), l);
+            if (whole) {
+              const int j = r / gq, h = kh * gq + r % gq;
+              float* dst = p.out + (((int64_t)b * M + j) * p.Hq + h) * kD + 16 * g;
+#pragma unroll
+              for (int md = 0; md < 8; ++md)
+                *reinterpret_cast<float2*>(dst + 2 * md) =
+                    make_float2(__fdiv_rn(o[md][nr][e], l), __fdiv_rn(o[md][nr][2 + e], l));
+            } else {
+              float* dst = part + (size_t)r * kD + 16 * g;
+#pragma unroll
+              for (int md = 0; md < 8; ++md)
+                *reinterpret_cast<float2*>(dst + 2 * md) = make_float2(o[md][nr][e], o[md][nr][2 + e]);
+              if (g == 0) {
+                part[(size_t)R * kD + r] = mwin[nr][e];
+                part[(size_t)R * kD + R + r] = l;
+              }
+            }
+          }
+      }
+    }
+
+    // ---- next item
+    t += G;
+    if (t >= total) break;
+    it0 = it1;
+    it1 = it2;
+    it2 = load_item(p, t + 2 * G, total);
+    sp = span_of(it0, kw, M, p.cap_rows);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ksp[e] = ksn[e];
+      vsp[e] = vsn[e];
+    }
+    load_span_scales(p, it1, span_of(it1, kw, M, p.cap_rows), lane, ksn, vsn);
+    qph ^= 1u;
+    if (pitem == 1) {
+      pitem = 0;                                  // the producer is already on this item
+    } else {
+      psp = sp;                                   // it had nothing left to read ahead
+      pblk = 0;
+    }
+    produce();
   }
 }
 
-// Merge of the 512-key windows of every (sequence, kv head) with more than one
-// window: M* = max_s m_s, w_s = e^(m_s - M*), out = sum_s w_s o_s / sum_s w_s l_s.
-// One CTA of 4 warps per (row, kv head, sequence), launched right after
-// decode_fast_kernel on the same stream (so every partial is in place).
-// Lane l covers channels 4l .. 4l+3; warp w takes windows s = w, w+4, ...
-// and sums them in window order; the 4 warp sums are added in warp order.
-// M* and l are block reductions in a fixed order.  Every step depends only
-// on the row's own windows, never on the batch.
-constexpr int kMergeWarps = 4;
+// ------------------------------------------------------------------- merge
+// Combination of the 512-key windows of every row whose sequence has more
+// than one window: out = sum_s w_s o_s / sum_s w_s l_s with w_s = e^(m_s - M*).
+// One CTA per (row, kv head, sequence).  Warp w takes windows w, w + 8, ...
+// in order and keeps a running (m, l, o) (lane l: channels 4l .. 4l+3); the
+// eight warp states are then combined in warp order.  Every step depends
+// only on the row's own windows, never on the batch.
+constexpr int kMergeWarps = 8;
 
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_windows_kernel(const DecodeParams p) {
-  __shared__ float red[kMergeWarps];
-  __shared__ float4 part_o[kMergeWarps][32];
+  __shared__ float wm[kMergeWarps], wl[kMergeWarps];
+  __shared__ float4 wo[kMergeWarps][32];
+  griddep_wait();                                 // every partial is in place
   const int r = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = p.R, gq = p.g;
@@ -681,61 +912,56 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_windows_kernel(const D
   const int ctx = p.ctx_len[b];
   if (!sequence_ok(rs, ctx, p.M, p.cap_rows, p.max_ctx)) return;   // NaN rows already written
   if (nsplit_for(ctx + p.M - 1) == 1) return;   // written directly by the decode kernel
-  const int ns = nsplit_for(ctx + r / gq);      // windows this row sees
-  const size_t pstride = (size_t)R * (kD + 2);
-  const size_t sstride = (size_t)p.Hkv * pstride;
-  const float* part0 = p.partials + ((size_t)b * p.nsplit_max * p.Hkv + kh) * pstride;
-  const float* mcol = part0 + (size_t)R * kD + r;   // m of window s at mcol + s * sstride
+  const int ns = nsplit_for(ctx + r / gq);      // the windows this row sees
+  const int pst = partial_stride(R);
+  const size_t sstride = (size_t)p.Hkv * pst;   // floats from one window to the next
+  const float* base = p.partials + ((size_t)b * p.nsplit_max * p.Hkv + kh) * pst;
+  const float* mcol = base + (size_t)R * kD + r;
   const float* lcol = mcol + R;
+  const float* ocol = base + (size_t)r * kD + 4 * lane;
 
-  // M*: thread t takes windows t, t + 128, ...; then warp and block maxima.
-  float mloc = -INFINITY;
-  for (int s = tid; s < ns; s += kMergeWarps * 32) mloc = fmaxf(mloc, __ldcg(mcol + s * sstride));
-  mloc = warp_max(mloc);
-  if (lane == 0) red[warp] = mloc;
-  __syncthreads();
-  float mstar = red[0];
-#pragma unroll
-  for (int w = 1; w < kMergeWarps; ++w) mstar = fmaxf(mstar, red[w]);
-  __syncthreads();
-
-  // l = sum_s w_s l_s: per-thread sums in window order, then warp butterflies,
-  // then warps in order.
-  float lloc = 0.0f;
-  for (int s = tid; s < ns; s += kMergeWarps * 32)
-    lloc = __fmaf_rn(exp_diff(__ldcg(mcol + s * sstride), mstar), __ldcg(lcol + s * sstride), lloc);
-  lloc = warp_sum(lloc);
-  if (lane == 0) red[warp] = lloc;
-
-  // o: warp w sums windows w, w + 4, ... in order (float4 per lane).
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* ocol = part0 + (size_t)r * kD + 4 * lane;
+  float m = -INFINITY, l = 0.0f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int s = warp; s < ns; s += kMergeWarps) {
-    const float w = exp_diff(__ldcg(mcol + s * sstride), mstar);
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(ocol + s * sstride));
-    acc.x = __fmaf_rn(w, v.x, acc.x);
-    acc.y = __fmaf_rn(w, v.y, acc.y);
-    acc.z = __fmaf_rn(w, v.z, acc.z);
-    acc.w = __fmaf_rn(w, v.w, acc.w);
+    const size_t off = (size_t)s * sstride;
+    const float ms = __ldcg(mcol + off), ls = __ldcg(lcol + off);
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(ocol + off));
+    const float mn = fmaxf(m, ms);
+    const float a = merge_weight(m, mn), w = merge_weight(ms, mn);
+    l = __fmaf_rn(ls, w, __fmul_rn(l, a));
+    o.x = __fmaf_rn(v.x, w, __fmul_rn(o.x, a));
+    o.y = __fmaf_rn(v.y, w, __fmul_rn(o.y, a));
+    o.z = __fmaf_rn(v.z, w, __fmul_rn(o.z, a));
+    o.w = __fmaf_rn(v.w, w, __fmul_rn(o.w, a));
+    m = mn;
   }
-  part_o[warp][lane] = acc;
+  if (lane == 0) {
+    wm[warp] = m;
+    wl[warp] = l;
+  }
+  wo[warp][lane] = o;
   __syncthreads();
   if (warp == 0) {
-    float l = red[0];
-    float4 o = part_o[0][lane];
+    float mstar = wm[0];
 #pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) {
-      l = __fadd_rn(l, red[w]);
-      const float4 v = part_o[w][lane];
-      o.x = __fadd_rn(o.x, v.x);
-      o.y = __fadd_rn(o.y, v.y);
-      o.z = __fadd_rn(o.z, v.z);
-      o.w = __fadd_rn(o.w, v.w);
+    for (int w = 1; w < kMergeWarps; ++w) mstar = fmaxf(mstar, wm[w]);
+    float lt = 0.0f;
+    float4 ot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) {
+      const float f = merge_weight(wm[w], mstar);
+      const float4 v = wo[w][lane];
+      lt = __fmaf_rn(wl[w], f, lt);
+      ot.x = __fmaf_rn(v.x, f, ot.x);
+      ot.y = __fmaf_rn(v.y, f, ot.y);
+      ot.z = __fmaf_rn(v.z, f, ot.z);
+      ot.w = __fmaf_rn(v.w, f, ot.w);
     }
     const int j = r / gq, h = kh * gq + r % gq;
     float4* dst = reinterpret_cast<float4*>(p.out + ((((int64_t)b * p.M + j) * p.Hq + h) * kD)) + lane;
-    *dst = make_float4(__fdiv_rn(o.x, l), __fdiv_rn(o.y, l), __fdiv_rn(o.z, l), __fdiv_rn(o.w, l));
+    *dst = make_float4(__fdiv_rn(ot.x, lt), __fdiv_rn(ot.y, lt), __fdiv_rn(ot.z, lt),
+                       __fdiv_rn(ot.w, lt));
   }
 }
 
@@ -767,15 +993,52 @@ bool encode_cache_map(CUtensorMap* map, const int8_t* base, int64_t rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous one on the stream drains; it waits (griddepcontrol.wait)
+// before it reads anything that one wrote.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+constexpr int kMaxDevices = 64;
+
 template <int NR, int NG, int PM>
 cudaError_t launch_variant(const DecodeParams& p, const TmaMaps& maps, cudaStream_t stream) {
   const int smem = (int)sizeof(SmemT<NR, NG>) + 1024;   // + alignment slack
+  constexpr int kThreads = kSpansPerCta * 32 * NG;
   const auto kern = decode_fast_kernel<NR, NG, PM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)p.nsplit_max, (unsigned)p.Hkv, (unsigned)p.B);
-  kern<<<grid, kSpansPerCta * 32 * NG, smem, stream>>>(p, maps);
-  return cudaGetLastError();
+  // Persistent grid: every CTA the GPU holds at once (cached per device).
+  static std::atomic<int> slots_cache[kMaxDevices];
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  int slots = (dev >= 0 && dev < kMaxDevices) ? slots_cache[dev].load() : 0;
+  if (slots <= 0) {
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem)) !=
+        cudaSuccess)
+      return e;
+    slots = sms * (per_sm > 0 ? per_sm : 1);
+    if (dev >= 0 && dev < kMaxDevices) slots_cache[dev].store(slots);
+  }
+  const int64_t items = (int64_t)p.B * p.nsplit_max * p.Hkv;   // an upper bound
+  const int grid = (int)(items < slots ? items : slots);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, stream, p, maps);
 }
 
 template <int NR, int NG>
@@ -795,15 +1058,22 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.Hkv * p.cap_rows;
   if (!encode_cache_map(&maps.k, p.k, rows) || !encode_cache_map(&maps.v, p.v, rows))
     return cudaErrorInvalidValue;
-  cudaError_t e;
+  // 1. packed queries and the work list (ordinary launch: it reads the
+  //    caller's q, row_start and ctx_len)
+  const int64_t qrows = (int64_t)p.B * p.Hkv * p.rpad;
+  const int q_blocks = (int)((qrows + kPrepWarps - 1) / kPrepWarps);
+  prepare_kernel<<<q_blocks + 1, kPrepWarps * 32, 0, stream>>>(p, q_blocks);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // 2. the split-KV pass
   if (p.R <= 8) e = launch_rows<1, 1>(p, maps, stream);
   else if (p.R <= 16) e = launch_rows<2, 1>(p, maps, stream);
   else if (p.R <= 32) e = launch_rows<4, 1>(p, maps, stream);
   else e = launch_rows<4, 2>(p, maps, stream);
   if (e != cudaSuccess || p.nsplit_max <= 1) return e;
-  merge_windows_kernel<<<dim3((unsigned)p.R, (unsigned)p.Hkv, (unsigned)p.B), kMergeWarps * 32, 0,
-                         stream>>>(p);
-  return cudaGetLastError();
+  // 3. the window merge
+  return launch_pdl(merge_windows_kernel, dim3((unsigned)p.R, (unsigned)p.Hkv, (unsigned)p.B),
+                    dim3(kMergeWarps * 32), 0, stream, p);
 }
 
 }  // namespace kattn

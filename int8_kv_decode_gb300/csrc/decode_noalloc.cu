@@ -80,12 +80,11 @@ extern "C" int kattn_decode_noalloc(const float* q, const int8_t* k, const float
   std::call_once(ds.once, [&ds] { ds.err = cudaGetSymbolAddress(&ds.ptr, g_scratch); });
   if (ds.err != cudaSuccess || ds.ptr == nullptr) return KATTN_ERR_CUDA;
 
-  // The array keeps whatever the previous call left in it.  The error word
-  // and the merge counters must start at zero; the partials are always
-  // written before they are read.
-  const kattn::WorkspaceLayout w = kattn::workspace_layout(B, M, Hq, max_ctx);
+  // The array keeps whatever the previous call left in it.  The header (the
+  // error word) must start at zero; the work list, the quantized queries and
+  // the partials are always written before they are read.
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ds.ptr, 0, w.partials_off, s) != cudaSuccess) return KATTN_ERR_CUDA;
+  if (cudaMemsetAsync(ds.ptr, 0, 256, s) != cudaSuccess) return KATTN_ERR_CUDA;
   return kattn_decode(q, k, k_scale, v, v_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows,
                       max_ctx, sm_scale, p_mode, 0, out, ds.ptr, kScratchBytes, stream);
 }

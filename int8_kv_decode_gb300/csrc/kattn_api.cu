@@ -57,6 +57,7 @@ DecodeParams make_params(const float* q, const int8_t* k, const float* k_scale,
   p.Hkv = Hkv;
   p.g = Hq / Hkv;
   p.R = p.g * M;
+  p.rpad = row_tile(p.R);
   p.cap_rows = cap_rows;
   p.max_ctx = max_ctx;
   p.nsplit_max = nsplit_for(max_ctx + M - 1);
@@ -157,11 +158,15 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale, const in
     e = launch_decode_exact(p, expf_constants(), as_stream(stream));
   } else {
     const WorkspaceLayout w = workspace_layout(B, M, Hq, max_ctx);
+    // work items x kv heads are counted in int32 on the device
+    if ((int64_t)B * w.nsplit_max * Hkv > (int64_t)INT32_MAX / 4) return KATTN_ERR_UNSUPPORTED;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
       return KATTN_ERR_WORKSPACE;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     p.err_word = reinterpret_cast<uint32_t*>(ws);
-    p.tickets = reinterpret_cast<uint32_t*>(ws + w.tickets_off);
+    p.item_count = reinterpret_cast<uint32_t*>(ws + 4);
+    p.items = reinterpret_cast<int4*>(ws + w.items_off);
+    p.qpack = ws + w.q_off;
     p.partials = reinterpret_cast<float*>(ws + w.partials_off);
     e = launch_decode_fast(p, as_stream(stream));
   }

@@ -26,27 +26,40 @@ static_assert(kSpanC % kBlockBk == 0, "a span is a whole number of blocks");
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- workspace
-// [0, 256)                   header: uint32 error word at offset 0
-// [256, 256 + T)             uint32 tickets, one per (b, kv head) -- B*Hq slots
-// [P0, ...)                  float partials per (b, split, kv head):
-//                            o[R][d], then m[R], then l[R]   (R = g*M rows)
+// [0, 256)      header: uint32 error word at byte 0, uint32 work-item count at 4
+// [I0, ...)     int4 work items {b, window, row_start, ctx}, one per 512-key
+//               window of every valid sequence: at most B * nsplit_max
+// [Q0, ...)     quantized queries per (b, kv head), rpad rows: rpad x 128 int8,
+//               then rpad float32 scales (rows >= R are zero)
+// [P0, ...)     float partials per (b, window, kv head): o[R][d], then m[R],
+//               then l[R], padded to a multiple of 4 floats (16-byte rows)
+// Only the header must be zero before the first call; the rest is written
+// by every call before it is read.
 struct WorkspaceLayout {
-  size_t tickets_off;
-  size_t partials_off;
-  size_t total;
+  size_t items_off, q_off, partials_off, total;
   int nsplit_max;
 };
 
 __host__ __device__ inline int nsplit_for(int keys) { return (keys + kSplitC - 1) / kSplitC; }
 
+// Query rows a decode CTA holds: R rounded up to the row tile of its variant.
+__host__ __device__ inline int row_tile(int R) { return R <= 8 ? 8 : R <= 16 ? 16 : R <= 32 ? 32 : 64; }
+__host__ __device__ inline int qpack_bytes(int rpad) { return rpad * (kD + 4); }
+__host__ __device__ inline int partial_stride(int R) { return R * kD + ((2 * R + 3) / 4) * 4; }
+
 inline WorkspaceLayout workspace_layout(int B, int M, int Hq, int max_ctx) {
+  // Bounds that hold for every Hkv dividing Hq (R = Hq / Hkv * M):
+  //   Hkv * row_tile(R) <= Hq * max(8, 2M);  Hkv * partial_stride(R) <= Hq * (M * 130 + 3).
   WorkspaceLayout w{};
   w.nsplit_max = nsplit_for(max_ctx + M - 1);
-  w.tickets_off = 256;
-  size_t tick = (size_t)B * (size_t)Hq * sizeof(uint32_t);
-  w.partials_off = (w.tickets_off + tick + 255) / 256 * 256;
-  size_t part = (size_t)B * (size_t)w.nsplit_max * (size_t)Hq * (size_t)M *
-                (size_t)(kD + 2) * sizeof(float);
+  const size_t nb = (size_t)B;
+  w.items_off = 256;
+  const size_t items = nb * (size_t)w.nsplit_max * 16;
+  w.q_off = (w.items_off + items + 255) / 256 * 256;
+  const size_t qb = nb * (size_t)Hq * (size_t)(M > 4 ? 2 * M : 8) * (size_t)(kD + 4);
+  w.partials_off = (w.q_off + qb + 255) / 256 * 256;
+  const size_t part = nb * (size_t)w.nsplit_max * (size_t)Hq * (size_t)(M * (kD + 2) + 3) *
+                      sizeof(float);
   w.total = (w.partials_off + part + 255) / 256 * 256;
   return w;
 }
@@ -61,9 +74,12 @@ struct DecodeParams {
   const int32_t* ctx_len;
   float* out;
   uint32_t* err_word;   // workspace header (fast mode), may be null in exact mode
-  uint32_t* tickets;    // [B][Hkv]
+  uint32_t* item_count; // workspace header + 4
+  int4* items;
+  uint8_t* qpack;
   float* partials;
   int B, M, Hq, Hkv, g, R;
+  int rpad;             // row_tile(R)
   int cap_rows, max_ctx, nsplit_max;
   float sm_scale;       // already resolved (never 0)
   int p_mode;

@@ -208,6 +208,44 @@ def test_shape_sweep(g, M):
     assert np.array_equal(bits(ex[m]), bits(ref[m]))
 
 
+@pytest.mark.parametrize("g,M", [(1, 3), (3, 1), (1, 5)])
+def test_odd_row_count_over_several_windows(g, M):
+    # R = g * M odd and sequences longer than one 512-key window: the
+    # per-window partial rows must stay 16-byte aligned for any R.
+    import int8_kv_decode_gb300 as K
+    ctxs = np.array([513, 1500, 2049, 700], np.int32)
+    wl = custom(f"odd_g{g}_m{M}", len(ctxs), M, 2 * g, 2, 1, outliers=True)
+    c = upload(wl, ctx_override=ctxs)
+    got = run(c).cpu().numpy()
+    assert_f32_tolerance(got, oracle_decode(c))
+    for j in range(M):
+        one = K.decode(c.q[:, j:j + 1].contiguous(), c.k8, c.ks, c.v8, c.vs, c.rs, c.ctx + j,
+                       c.x.max_ctx + j).cpu().numpy()
+        assert np.array_equal(bits(got[:, j:j + 1]), bits(one))
+
+
+def test_decode_replays_in_a_cuda_graph():
+    # The three launches of a fast decode, captured once and replayed, give
+    # the bytes of an ordinary call.
+    import torch
+    import int8_kv_decode_gb300 as K
+    c = upload(WORKLOADS["spec_verify"])
+    B, M, Hq, _ = c.q.shape
+    ws = K.alloc_workspace(B, M, Hq, c.x.max_ctx)
+    ref = run(c, workspace=ws).cpu().numpy()
+    out = torch.full_like(c.q, float("nan"))
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+        K.decode(c.q, c.k8, c.ks, c.v8, c.vs, c.rs, c.ctx, c.x.max_ctx, out=out, workspace=ws)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out.cpu().numpy()), bits(ref))
+
+
 def test_bad_sequence_is_flagged_without_touching_other_rows():
     import torch
     import int8_kv_decode_gb300 as K
