@@ -54,9 +54,10 @@ def qo_bytes(B: int, M: int, Hq: int, d: int = HEAD_DIM) -> int:
 
 
 def decode_launches(max_ctx: int, M: int) -> int:
-    """Kernels one fast-mode kattn_decode launches: the split-KV pass, plus
-    the window merge when the longest row spans more than one 512-key window."""
-    return 1 + (int(max_ctx) + M - 1 > 512)
+    """Kernels one fast-mode kattn_decode launches: query packing, the work
+    list and the split-KV pass, plus the window merge when the longest row
+    spans more than one 512-key window."""
+    return 3 + (int(max_ctx) + M - 1 > 512)
 
 
 def append_rows(row_start, ctx, M: int):

@@ -1,12 +1,13 @@
 // Fast decode over the int8 KV cache: split-KV on tensor cores, fixed-order merge.
 //
-// Three launches on the caller's stream, chained by programmatic dependent
+// Four launches on the caller's stream, chained by programmatic dependent
 // launch (a kernel starts while the previous one drains and waits on
 // griddepcontrol before it reads that one's results):
 //   1. prepare_kernel quantizes every query row once (int8 per row) into the
-//      workspace and lists the work items of the valid sequences, one per
-//      window of kSplitC = 512 keys; the rows of an invalid sequence become
-//      NaN and raise an error bit;
+//      workspace and counts the work items of the valid sequences, one per
+//      window of kSplitC = 512 keys and kv head (a prefix over sequences);
+//      the rows of an invalid sequence become NaN and raise an error bit;
+//   1b. list_kernel writes the work items, one thread each;
 //   2. decode_fast_kernel: persistent CTAs (SM count x occupancy) take the
 //      items x kv heads in a fixed stride.  In a CTA, warp kw reduces span kw
 //      (kSpanC = 128 keys) of the window for all R = g*M query rows that read
@@ -46,6 +47,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "device_common.cuh"
@@ -252,17 +254,21 @@ __device__ __forceinline__ void named_arrive(int id, int threads) {
 }
 
 // ------------------------------------------------------------ work items
-// Work item t of the decode grid: window items[t / Hkv] of a sequence, kv
-// head t % Hkv.  b < 0 marks "no item".
+// Work item t of the decode grid is one (sequence b, window w, kv head kh):
+// the items of sequence b are t in [prefix[b], prefix[b + 1]), windows in
+// order, kv heads fastest.  list_kernel stores each as {b | kh << 16, w,
+// kh * cap_rows + row_start[b], ctx_len[b]}: row is the cache row of key 0 of
+// the sequence in the 2-D view [Hkv * cap_rows][128] (and the index of its
+// scales).  b < 0 marks "no item".
 struct Item {
-  int b, w, rs, ctx, kh;
+  int b, kh, w, row, ctx;
 };
 
 __device__ __forceinline__ Item load_item(const DecodeParams& p, int t, int total) {
   Item it{-1, 0, 0, 0, 0};
   if (t < total) {
-    const int4 v = __ldcg(p.items + t / p.Hkv);
-    it = Item{v.x, v.y, v.z, v.w, t % p.Hkv};
+    const int4 v = __ldcg(p.items + t);
+    it = Item{v.x & 0xffff, (int)((unsigned)v.x >> 16), v.y, v.z, v.w};
   }
   return it;
 }
@@ -273,14 +279,14 @@ struct Span {
   int s0, s1, nb, row;
 };
 
-__device__ __forceinline__ Span span_of(const Item& it, int kw, int M, int cap_rows) {
+__device__ __forceinline__ Span span_of(const Item& it, int kw, int M) {
   Span s;
   const int Lmax = it.ctx + M - 1;
   const int k0 = it.w * kSplitC, k1 = min(k0 + kSplitC, Lmax);
   s.s0 = k0 + kw * kSpanC;
   s.s1 = min(s.s0 + kSpanC, k1);
   s.nb = s.s1 > s.s0 ? (s.s1 - s.s0 + kBlockBk - 1) / kBlockBk : 0;
-  s.row = it.kh * cap_rows + it.rs + s.s0;
+  s.row = it.row + s.s0;
   return s;
 }
 
@@ -288,20 +294,19 @@ __device__ __forceinline__ Span span_of(const Item& it, int kw, int M, int cap_r
 __device__ __forceinline__ void load_span_scales(const DecodeParams& p, const Item& it,
                                                  const Span& sp, int lane, float (&ks)[4],
                                                  float (&vs)[4]) {
-  const int64_t base = (int64_t)it.kh * p.cap_rows + it.rs;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int key = sp.s0 + lane + 32 * e;
     const bool in = it.b >= 0 && key < sp.s1;
-    ks[e] = in ? __ldg(p.k_scale + base + key) : 0.0f;
-    vs[e] = in ? __ldg(p.v_scale + base + key) : 0.0f;
+    ks[e] = in ? __ldg(p.k_scale + it.row + key) : 0.0f;
+    vs[e] = in ? __ldg(p.v_scale + it.row + key) : 0.0f;
   }
 }
 
 // ------------------------------------------------------------------ prepare
 // Blocks [0, q_blocks): one warp per packed query row (b, kv head, r < rpad):
 // row r < R is query (column j = r / g, head kh * g + r % g) quantized per
-// row, rows r >= R are zero.  The last block lists the work items.
+// row, rows r >= R are zero.  The last block writes the work-item prefix.
 constexpr int kPrepWarps = 4;
 
 __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodeParams p,
@@ -332,39 +337,62 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodePa
     if (lane == 0) reinterpret_cast<float*>(pack + p.rpad * kD)[r] = s;
     return;
   }
-  // The work list: sequences in order, windows in order.
-  __shared__ int warp_total[kPrepWarps];
-  int base = 0;
-  for (int b0 = 0; b0 < p.B; b0 += kPrepWarps * 32) {
-    const int b = b0 + tid;
-    int nw = 0, rs = 0, ctx = 0;
-    if (b < p.B) {
-      const int64_t rs64 = p.row_start[b];
-      ctx = p.ctx_len[b];
-      if (sequence_ok(rs64, ctx, p.M, p.cap_rows, p.max_ctx)) {
-        nw = nsplit_for(ctx + p.M - 1);
-        rs = (int)rs64;                            // < cap_rows: fits
-      }
-    }
-    int incl = nw;                                 // inclusive warp scan
+  // The last block: prefix[b] = work items (windows x kv heads) of the valid
+  // sequences before b.  Thread i takes a run of consecutive sequences,
+  // counts them, the runs are scanned across the block, and each thread
+  // writes its run.
+  constexpr int kThreads = kPrepWarps * 32;
+  __shared__ int s_warp[kPrepWarps];
+  auto items_of = [&](int b) -> int {
+    const int64_t rs = p.row_start[b];
+    const int ctx = p.ctx_len[b];
+    return sequence_ok(rs, ctx, p.M, p.cap_rows, p.max_ctx) ? nsplit_for(ctx + p.M - 1) * p.Hkv
+                                                             : 0;
+  };
+  const int per = (p.B + kThreads - 1) / kThreads;
+  const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
+  int run = 0;
+  for (int b = b_lo; b < b_hi; ++b) run += items_of(b);
+  int incl = run;                                 // inclusive scan over the block
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_total[warp] = incl;
-    __syncthreads();
-    int off = base + incl - nw, chunk = 0;
-#pragma unroll
-    for (int w = 0; w < kPrepWarps; ++w) {
-      if (w < warp) off += warp_total[w];
-      chunk += warp_total[w];
-    }
-    __syncthreads();
-    for (int w = 0; w < nw; ++w) p.items[off + w] = make_int4(b, w, rs, ctx);
-    base += chunk;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
   }
-  if (tid == 0) *p.item_count = (uint32_t)base;
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int base = incl - run;
+#pragma unroll
+  for (int w = 0; w < kPrepWarps; ++w)
+    if (w < warp) base += s_warp[w];
+  for (int b = b_lo; b < b_hi; ++b) {
+    p.prefix[b] = base;
+    base += items_of(b);
+  }
+  if (tid == kThreads - 1) {                      // its run ends at B
+    p.prefix[p.B] = base;
+    *p.item_count = (uint32_t)base;
+  }
+}
+
+// One thread per work item (grid-stride): b by binary search over prefix.
+constexpr int kListThreads = 256;
+
+__global__ void __launch_bounds__(kListThreads) list_kernel(const DecodeParams p) {
+  griddep_wait();                                 // prefix and the count
+  griddep_launch_dependents();
+  const int total = (int)__ldcg(p.item_count);
+  for (int j = blockIdx.x * kListThreads + threadIdx.x; j < total; j += gridDim.x * kListThreads) {
+    int lo = 0, hi = p.B;                         // prefix[lo] <= j < prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldcg(p.prefix + mid) <= j) lo = mid;
+      else hi = mid;
+    }
+    const int i = j - __ldcg(p.prefix + lo), w = i / p.Hkv, kh = i - w * p.Hkv;
+    p.items[j] = make_int4(lo | (kh << 16), w, kh * p.cap_rows + (int)p.row_start[lo],
+                           p.ctx_len[lo]);
+  }
 }
 
 // ------------------------------------------------------------------ decode
@@ -396,6 +424,18 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   const int gq = p.g, M = p.M, R = p.R;
   const int row0 = grp * RG;
   uint64_t* full = sm.full[warp];
+  // Per thread and fixed for the launch: the draft column j of rows
+  // 8nr + 2c + e of the group, and where those rows sit in out (head kh * g
+  // + r % g; add kh * g * d and the sequence's offset).
+  int jrow[NR][2], orow[NR][2];
+#pragma unroll
+  for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = row0 + nr * 8 + 2 * c + e;
+      jrow[nr][e] = min(r / gq, M - 1);
+      orow[nr][e] = ((r / gq) * p.Hq + r % gq) * kD + 16 * g;
+    }
 
   if (lane == 0) {
     for (int s = 0; s < kRing; ++s) mbar_init(&full[s], 1);
@@ -407,7 +447,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   griddep_wait();                                 // the work list and the packed queries
   griddep_launch_dependents();
 
-  const int total = (int)__ldcg(p.item_count) * p.Hkv;
+  const int total = (int)__ldcg(p.item_count);
   const int G = gridDim.x;
   int t = blockIdx.x;
   if (t >= total) return;
@@ -425,7 +465,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 
   // ---- producer: lane 0 issues, every lane keeps the same counters.  The
   // cursor runs over this item's blocks, then the next item's.
-  Span psp = span_of(it0, kw, M, p.cap_rows);
+  Span psp = span_of(it0, kw, M);
   int pitem = 0, pblk = 0, ist = 0, inflight = 0;
   auto produce = [&]() {
     while (inflight < kRing) {
@@ -443,7 +483,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
       } else if (pitem == 0 && it1.b >= 0) {
         pitem = 1;
         pblk = 0;
-        psp = span_of(it1, kw, M, p.cap_rows);
+        psp = span_of(it1, kw, M);
       } else {
         break;
       }
@@ -452,10 +492,10 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   produce();
 
   // ---- consumer state
-  Span sp = span_of(it0, kw, M, p.cap_rows);
+  Span sp = span_of(it0, kw, M);
   float ksp[4], vsp[4], ksn[4], vsn[4];           // this item's / the next item's span scales
   load_span_scales(p, it0, sp, lane, ksp, vsp);
-  load_span_scales(p, it1, span_of(it1, kw, M, p.cap_rows), lane, ksn, vsn);
+  load_span_scales(p, it1, span_of(it1, kw, M), lane, ksn, vsn);
   int cst = 0;                                    // ring stage of the next block to consume
   uint32_t cph = 0, qph = 0;                      // its mbarrier parity; the query barrier's
 
@@ -511,27 +551,28 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
       for (int e = 0; e < 4; ++e)
         if (sp.s0 + lane + 32 * e < kc) vm = fmaxf(vm, vsp[e]);
       vm = warp_max(vm);
-      float vt[kMaxM - 1];                       // scales of keys ctx + t (the draft tail)
+      float vt[kMaxM - 1];                        // scales of keys ctx + t (the draft tail)
 #pragma unroll
-      for (int t = 0; t < kMaxM - 1; ++t) {
-        const int rel = ctx + t - sp.s0;          // uniform over the warp
-        float v = 0.0f;
-        if (t < M - 1 && rel >= 0 && ctx + t < sp.s1) {
-          const int e = rel >> 5;
-          const float mine = e == 0 ? vsp[0] : e == 1 ? vsp[1] : e == 2 ? vsp[2] : vsp[3];
-          v = __shfl_sync(0xffffffffu, mine, rel & 31);
+      for (int t = 0; t < kMaxM - 1; ++t) vt[t] = 0.0f;
+      if (sp.s1 > ctx) {                          // the span holds draft keys (uniform)
+#pragma unroll
+        for (int t = 0; t < kMaxM - 1; ++t) {
+          const int rel = ctx + t - sp.s0;
+          if (t < M - 1 && rel >= 0 && ctx + t < sp.s1) {
+            const int e = rel >> 5;
+            const float mine = e == 0 ? vsp[0] : e == 1 ? vsp[1] : e == 2 ? vsp[2] : vsp[3];
+            vt[t] = __shfl_sync(0xffffffffu, mine, rel & 31);
+          }
         }
-        vt[t] = v;
       }
 #pragma unroll
       for (int nr = 0; nr < NR; ++nr)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int jr = min((row0 + nr * 8 + 2 * c + e) / gq, M - 1);
           float vmax = vm;
 #pragma unroll
           for (int t = 0; t < kMaxM - 1; ++t)
-            if (t < jr) vmax = fmaxf(vmax, vt[t]);
+            if (t < jrow[nr][e]) vmax = fmaxf(vmax, vt[t]);
           const int bexp = min(max(268 - (int)((__float_as_uint(vmax) >> 23) & 0xffu), 1), 253);
           up_row[nr][e] = __uint_as_float((uint32_t)bexp << 23);
           down_row[nr][e] = __uint_as_float((uint32_t)(254 - bexp) << 23);
@@ -547,7 +588,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
       for (int e = 0; e < 2; ++e) {
         m_run[nr][e] = -INFINITY;
         l_run[nr][e] = 0.0f;
-        Lrow[nr][e] = ctx + min((row0 + nr * 8 + 2 * c + e) / gq, M - 1);
+        Lrow[nr][e] = ctx + jrow[nr][e];
       }
     float o[8][NR][4];
 #pragma unroll
@@ -619,8 +660,9 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
         }
       }
 
-      // ---- scores s = ((S * (qs * ks)) * sm_scale), masked past each row's L
-      const bool all_visible = t0 + kBlockBk <= ctx;   // ctx is the smallest L of any row
+      // ---- scores s = ((S * (qs * ks)) * sm_scale), rounded as written,
+      // masked past each row's L (only the last block of a sequence has keys
+      // some row does not see)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
@@ -631,10 +673,20 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
             const float2 qk = f2_mul(make_float2(qs_row[nr][0], qs_row[nr][1]), make_float2(ksv, ksv));
             float2 s2 = f2_mul(make_float2(sc[hf][nr][2 * k2], sc[hf][nr][2 * k2 + 1]), qk);
             s2 = f2_mul(s2, make_float2(p.sm_scale, p.sm_scale));
-            const int key = t0 + 16 * hf + g + 8 * k2;
-            sc[hf][nr][2 * k2] = (all_visible || key < Lrow[nr][0]) ? s2.x : -INFINITY;
-            sc[hf][nr][2 * k2 + 1] = (all_visible || key < Lrow[nr][1]) ? s2.y : -INFINITY;
+            sc[hf][nr][2 * k2] = s2.x;
+            sc[hf][nr][2 * k2 + 1] = s2.y;
           }
+      if (t0 + kBlockBk > ctx) {                    // ctx is the smallest L of any row
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int nr = 0; nr < NR; ++nr)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int key = t0 + 16 * hf + g + 8 * (u >> 1);
+              if (key >= Lrow[nr][u & 1]) sc[hf][nr][u] = -INFINITY;
+            }
+      }
 
       // ---- online softmax update of rows 8nr + 2c + e over the 32-key block
       float alpha[NR][2];
@@ -848,8 +900,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
             for (int w = 0; w < kSpansPerCta; ++w)
               l = __fmaf_rn(sm.wl[grp][w][rr], merge_weight(sm.wm[grp][w][rr], mwin[nr][e]), l);
             if (whole) {
-              const int j = r / gq, h = kh * gq + r % gq;
-              float* dst = p.out + (((int64_t)b * M + j) * p.Hq + h) * kD + 16 * g;
+              float* dst = p.out + ((int64_t)b * M * p.Hq + kh * gq) * kD + orow[nr][e];
 #pragma unroll
               for (int md = 0; md < 8; ++md)
                 *reinterpret_cast<float2*>(dst + 2 * md) =
@@ -874,13 +925,13 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     it0 = it1;
     it1 = it2;
     it2 = load_item(p, t + 2 * G, total);
-    sp = span_of(it0, kw, M, p.cap_rows);
+    sp = span_of(it0, kw, M);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       ksp[e] = ksn[e];
       vsp[e] = vsn[e];
     }
-    load_span_scales(p, it1, span_of(it1, kw, M, p.cap_rows), lane, ksn, vsn);
+    load_span_scales(p, it1, span_of(it1, kw, M), lane, ksn, vsn);
     qph ^= 1u;
     if (pitem == 1) {
       pitem = 0;                                  // the producer is already on this item
@@ -894,20 +945,52 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 
 // ------------------------------------------------------------------- merge
 // Combination of the 512-key windows of every row whose sequence has more
-// than one window: out = sum_s w_s o_s / sum_s w_s l_s with w_s = e^(m_s - M*).
-// One CTA per (row, kv head, sequence).  Warp w takes windows w, w + 8, ...
-// in order and keeps a running (m, l, o) (lane l: channels 4l .. 4l+3); the
-// eight warp states are then combined in warp order.  Every step depends
-// only on the row's own windows, never on the batch.
+// than one window.  A state (m, l, o) merges with (m', l', o') into
+// (M, l e^(m-M) + l' e^(m'-M), o e^(m-M) + o' e^(m'-M)), M = max(m, m').
+// The order is fixed by the row's own window count ns: window s goes to
+// slot s mod 32, each slot folds its windows in order, then the 32 slots
+// are folded in order (for ns <= 32: the windows folded in order); the row
+// is o / l.  Which warps do the work does not change a single rounding, so
+// the same order serves short rows (one warp per row, eight rows per CTA,
+// slot by slot) and long ones (eight warps per row, four slots each).
 constexpr int kMergeWarps = 8;
+constexpr int kMergeSlots = 32;
 
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_windows_kernel(const DecodeParams p) {
-  __shared__ float wm[kMergeWarps], wl[kMergeWarps];
-  __shared__ float4 wo[kMergeWarps][32];
+struct MergeState {
+  float m, l;
+  float4 o;
+};
+
+// One of the two weights is e^0 = 1 exactly, so only the other is taken
+// from ex2; the rounding steps are those of the formula above.
+__device__ __forceinline__ void merge_into(MergeState& st, float m2, float l2, float4 o2) {
+  const float mn = fmaxf(st.m, m2);
+  float a = 1.0f, w = 1.0f;
+  if (st.m < m2) a = merge_weight(st.m, mn);
+  else w = merge_weight(m2, mn);
+  st.l = __fmaf_rn(l2, w, __fmul_rn(st.l, a));
+  st.o.x = __fmaf_rn(o2.x, w, __fmul_rn(st.o.x, a));
+  st.o.y = __fmaf_rn(o2.y, w, __fmul_rn(st.o.y, a));
+  st.o.z = __fmaf_rn(o2.z, w, __fmul_rn(st.o.z, a));
+  st.o.w = __fmaf_rn(o2.w, w, __fmul_rn(st.o.w, a));
+  st.m = mn;
+}
+
+// WPR warps per row (1 or kMergeWarps); lane l covers channels 4l .. 4l+3.
+// Grid (rows of one sequence / rows per CTA, B): blockIdx.y is the sequence.
+template <int WPR>
+__global__ void __launch_bounds__(kMergeWarps * 32, WPR == 1 ? 3 : 1)
+merge_windows_kernel(const DecodeParams p) {
+  constexpr int kSlotsPerWarp = kMergeSlots / WPR;
+  __shared__ float sm_m[WPR == 1 ? 1 : kMergeSlots], sm_l[WPR == 1 ? 1 : kMergeSlots];
+  __shared__ float4 sm_o[WPR == 1 ? 1 : kMergeSlots][32];
   griddep_wait();                                 // every partial is in place
-  const int r = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = p.R, gq = p.g;
+  const int b = blockIdx.y;
+  const int row = WPR == 1 ? (int)blockIdx.x * kMergeWarps + warp : (int)blockIdx.x;   // kh * R + r
+  if (row >= p.Hkv * R) return;
+  const int kh = row / R, r = row - kh * R;
   const int64_t rs = p.row_start[b];
   const int ctx = p.ctx_len[b];
   if (!sequence_ok(rs, ctx, p.M, p.cap_rows, p.max_ctx)) return;   // NaN rows already written
@@ -919,50 +1002,73 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_windows_kernel(const D
   const float* mcol = base + (size_t)R * kD + r;
   const float* lcol = mcol + R;
   const float* ocol = base + (size_t)r * kD + 4 * lane;
-
-  float m = -INFINITY, l = 0.0f;
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int s = warp; s < ns; s += kMergeWarps) {
+  auto load = [&](int s, float& m2, float& l2, float4& o2) {
     const size_t off = (size_t)s * sstride;
-    const float ms = __ldcg(mcol + off), ls = __ldcg(lcol + off);
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(ocol + off));
-    const float mn = fmaxf(m, ms);
-    const float a = merge_weight(m, mn), w = merge_weight(ms, mn);
-    l = __fmaf_rn(ls, w, __fmul_rn(l, a));
-    o.x = __fmaf_rn(v.x, w, __fmul_rn(o.x, a));
-    o.y = __fmaf_rn(v.y, w, __fmul_rn(o.y, a));
-    o.z = __fmaf_rn(v.z, w, __fmul_rn(o.z, a));
-    o.w = __fmaf_rn(v.w, w, __fmul_rn(o.w, a));
-    m = mn;
-  }
-  if (lane == 0) {
-    wm[warp] = m;
-    wl[warp] = l;
-  }
-  wo[warp][lane] = o;
-  __syncthreads();
-  if (warp == 0) {
-    float mstar = wm[0];
+    m2 = __ldcg(mcol + off);
+    l2 = __ldcg(lcol + off);
+    o2 = __ldcg(reinterpret_cast<const float4*>(ocol + off));
+  };
+
+  MergeState fin{-INFINITY, 0.0f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  if constexpr (WPR == 1) {
+    // ns <= 64: slot k holds window k and, when k + 32 < ns, window k + 32.
+    // A batch of slots has all its loads in flight before it is folded.
+    constexpr int kBatch = 4;
+    const int nk = min(ns, kMergeSlots);
+    for (int k0 = 0; k0 < nk; k0 += kBatch) {
+      float m1[kBatch], l1[kBatch], m2[kBatch], l2[kBatch];
+      float4 o1[kBatch], o2[kBatch];
 #pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w) mstar = fmaxf(mstar, wm[w]);
-    float lt = 0.0f;
-    float4 ot = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < kBatch; ++i) {
+        if (k0 + i < nk) load(k0 + i, m1[i], l1[i], o1[i]);
+        if (k0 + i + kMergeSlots < ns) load(k0 + i + kMergeSlots, m2[i], l2[i], o2[i]);
+      }
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) {
-      const float f = merge_weight(wm[w], mstar);
-      const float4 v = wo[w][lane];
-      lt = __fmaf_rn(wl[w], f, lt);
-      ot.x = __fmaf_rn(v.x, f, ot.x);
-      ot.y = __fmaf_rn(v.y, f, ot.y);
-      ot.z = __fmaf_rn(v.z, f, ot.z);
-      ot.w = __fmaf_rn(v.w, f, ot.w);
+      for (int i = 0; i < kBatch; ++i) {
+        if (k0 + i < nk) {
+          MergeState st{m1[i], l1[i], o1[i]};     // = the empty state merged with it
+          if (k0 + i + kMergeSlots < ns) merge_into(st, m2[i], l2[i], o2[i]);
+          if (k0 + i == 0) fin = st;
+          else merge_into(fin, st.m, st.l, st.o);
+        }
+      }
     }
-    const int j = r / gq, h = kh * gq + r % gq;
-    float4* dst = reinterpret_cast<float4*>(p.out + ((((int64_t)b * p.M + j) * p.Hq + h) * kD)) + lane;
-    *dst = make_float4(__fdiv_rn(ot.x, lt), __fdiv_rn(ot.y, lt), __fdiv_rn(ot.z, lt),
-                       __fdiv_rn(ot.w, lt));
+  } else {
+    // this warp's slots k = warp * kSlotsPerWarp + i, each folding s = k, k + 32, ...
+    MergeState st[kSlotsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kSlotsPerWarp; ++i) st[i] = MergeState{-INFINITY, 0.0f, make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int s0 = 0; s0 < ns; s0 += kMergeSlots) {
+#pragma unroll
+      for (int i = 0; i < kSlotsPerWarp; ++i) {
+        const int s = s0 + warp * kSlotsPerWarp + i;
+        if (s < ns) {
+          float m2, l2;
+          float4 o2;
+          load(s, m2, l2, o2);
+          if (s0 == 0) st[i] = MergeState{m2, l2, o2};   // = the empty state merged with it
+          else merge_into(st[i], m2, l2, o2);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kSlotsPerWarp; ++i) {
+      const int k = warp * kSlotsPerWarp + i;
+      if (lane == 0) {
+        sm_m[k] = st[i].m;
+        sm_l[k] = st[i].l;
+      }
+      sm_o[k][lane] = st[i].o;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    fin = MergeState{sm_m[0], sm_l[0], sm_o[0][lane]};
+    for (int k = 1; k < kMergeSlots && k < ns; ++k) merge_into(fin, sm_m[k], sm_l[k], sm_o[k][lane]);
   }
+  const int j = r / gq, h = kh * gq + (r - j * gq);
+  float4* dst = reinterpret_cast<float4*>(p.out + ((((int64_t)b * p.M + j) * p.Hq + h) * kD)) + lane;
+  *dst = make_float4(__fdiv_rn(fin.o.x, fin.l), __fdiv_rn(fin.o.y, fin.l), __fdiv_rn(fin.o.z, fin.l),
+                     __fdiv_rn(fin.o.w, fin.l));
 }
 
 // ------------------------------------------------------------------- host
@@ -1065,14 +1171,25 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
   prepare_kernel<<<q_blocks + 1, kPrepWarps * 32, 0, stream>>>(p, q_blocks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  const int64_t max_items = (int64_t)p.B * p.nsplit_max * p.Hkv;
+  const int list_blocks = (int)std::min<int64_t>((max_items + kListThreads - 1) / kListThreads, 4096);
+  if ((e = launch_pdl(list_kernel, dim3((unsigned)list_blocks), dim3(kListThreads), 0, stream, p)) !=
+      cudaSuccess)
+    return e;
   // 2. the split-KV pass
   if (p.R <= 8) e = launch_rows<1, 1>(p, maps, stream);
   else if (p.R <= 16) e = launch_rows<2, 1>(p, maps, stream);
   else if (p.R <= 32) e = launch_rows<4, 1>(p, maps, stream);
   else e = launch_rows<4, 2>(p, maps, stream);
   if (e != cudaSuccess || p.nsplit_max <= 1) return e;
-  // 3. the window merge
-  return launch_pdl(merge_windows_kernel, dim3((unsigned)p.R, (unsigned)p.Hkv, (unsigned)p.B),
+  // 3. the window merge: one warp per row while no row has more than 64
+  //    windows, else eight warps per row (the same arithmetic either way)
+  const int rows_b = p.Hkv * p.R;                 // rows of one sequence
+  if (p.nsplit_max <= 2 * kMergeSlots)
+    return launch_pdl(merge_windows_kernel<1>,
+                      dim3((unsigned)((rows_b + kMergeWarps - 1) / kMergeWarps), (unsigned)p.B),
+                      dim3(kMergeWarps * 32), 0, stream, p);
+  return launch_pdl(merge_windows_kernel<kMergeWarps>, dim3((unsigned)rows_b, (unsigned)p.B),
                     dim3(kMergeWarps * 32), 0, stream, p);
 }
 

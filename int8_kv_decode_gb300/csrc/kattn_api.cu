@@ -165,6 +165,7 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale, const in
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     p.err_word = reinterpret_cast<uint32_t*>(ws);
     p.item_count = reinterpret_cast<uint32_t*>(ws + 4);
+    p.prefix = reinterpret_cast<int*>(ws + w.prefix_off);
     p.items = reinterpret_cast<int4*>(ws + w.items_off);
     p.qpack = ws + w.q_off;
     p.partials = reinterpret_cast<float*>(ws + w.partials_off);

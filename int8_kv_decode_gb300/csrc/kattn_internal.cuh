@@ -27,8 +27,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- workspace
 // [0, 256)      header: uint32 error word at byte 0, uint32 work-item count at 4
-// [I0, ...)     int4 work items {b, window, row_start, ctx}, one per 512-key
-//               window of every valid sequence: at most B * nsplit_max
+// [X0, ...)     int32 prefix[B + 1]: work items (512-key window x kv head) of
+//               the valid sequences before sequence b; prefix[B] is the total
+// [I0, ...)     int4 work items, one per (valid sequence, window, kv head):
+//               at most B * nsplit_max * Hkv <= B * nsplit_max * Hq
 // [Q0, ...)     quantized queries per (b, kv head), rpad rows: rpad x 128 int8,
 //               then rpad float32 scales (rows >= R are zero)
 // [P0, ...)     float partials per (b, window, kv head): o[R][d], then m[R],
@@ -36,7 +38,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Only the header must be zero before the first call; the rest is written
 // by every call before it is read.
 struct WorkspaceLayout {
-  size_t items_off, q_off, partials_off, total;
+  size_t prefix_off, items_off, q_off, partials_off, total;
   int nsplit_max;
 };
 
@@ -53,8 +55,9 @@ inline WorkspaceLayout workspace_layout(int B, int M, int Hq, int max_ctx) {
   WorkspaceLayout w{};
   w.nsplit_max = nsplit_for(max_ctx + M - 1);
   const size_t nb = (size_t)B;
-  w.items_off = 256;
-  const size_t items = nb * (size_t)w.nsplit_max * 16;
+  w.prefix_off = 256;
+  w.items_off = (w.prefix_off + (nb + 1) * sizeof(int) + 255) / 256 * 256;
+  const size_t items = nb * (size_t)w.nsplit_max * (size_t)Hq * 16;
   w.q_off = (w.items_off + items + 255) / 256 * 256;
   const size_t qb = nb * (size_t)Hq * (size_t)(M > 4 ? 2 * M : 8) * (size_t)(kD + 4);
   w.partials_off = (w.q_off + qb + 255) / 256 * 256;
@@ -75,6 +78,7 @@ struct DecodeParams {
   float* out;
   uint32_t* err_word;   // workspace header (fast mode), may be null in exact mode
   uint32_t* item_count; // workspace header + 4
+  int* prefix;          // [B + 1]
   int4* items;
   uint8_t* qpack;
   float* partials;
