@@ -118,13 +118,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// L2 policy for the K/V stream: read once, so its lines go first and the
+// window partials written meanwhile stay in L2 for the merge.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+
 // kBlockBk rows x 128 bytes starting at row `row` of a 2-D cache view.
 __device__ __forceinline__ void tma_load_block(void* dst, const CUtensorMap* map, int row,
-                                               uint64_t* bar) {
+                                               uint64_t* bar, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(0), "r"(row), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(0), "r"(row), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 
@@ -467,6 +475,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   // cursor runs over this item's blocks, then the next item's.
   Span psp = span_of(it0, kw, M);
   int pitem = 0, pblk = 0, ist = 0, inflight = 0;
+  const uint64_t kv_policy = l2_evict_first();
   auto produce = [&]() {
     while (inflight < kRing) {
       if (pblk < psp.nb) {
@@ -474,8 +483,8 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
           asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
           mbar_expect_tx(&full[ist], 2 * kBlockBytes);
           const int row = psp.row + pblk * kBlockBk;
-          tma_load_block(sm.ring[warp][ist][0], &maps.k, row, &full[ist]);
-          tma_load_block(sm.ring[warp][ist][1], &maps.v, row, &full[ist]);
+          tma_load_block(sm.ring[warp][ist][0], &maps.k, row, &full[ist], kv_policy);
+          tma_load_block(sm.ring[warp][ist][1], &maps.v, row, &full[ist], kv_policy);
         }
         ++pblk;
         ++inflight;
@@ -945,50 +954,30 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 
 // ------------------------------------------------------------------- merge
 // Combination of the 512-key windows of every row whose sequence has more
-// than one window.  A state (m, l, o) merges with (m', l', o') into
-// (M, l e^(m-M) + l' e^(m'-M), o e^(m-M) + o' e^(m'-M)), M = max(m, m').
-// The order is fixed by the row's own window count ns: window s goes to
-// slot s mod 32, each slot folds its windows in order, then the 32 slots
-// are folded in order (for ns <= 32: the windows folded in order); the row
-// is o / l.  Which warps do the work does not change a single rounding, so
-// the same order serves short rows (one warp per row, eight rows per CTA,
-// slot by slot) and long ones (eight warps per row, four slots each).
-constexpr int kMergeWarps = 8;
+// than one window, in an order fixed by the row's own window count ns:
+//   M  = max_s m_s,  w_s = e^(m_s - M)
+//   slot k (window s goes to slot s mod 32) sums w_s o_s and w_s l_s over
+//   its windows in order (first term a product, then fused adds);
+//   O  = the slot sums of o added in slot order;
+//   L  = the slot sums of l added by the butterfly of warp_sum (lane k = slot k);
+//   out = O / L.
+// Which warps do the work does not change a single rounding, so the same
+// order serves many short rows (one warp per row, lane k = slot k, ns <= 64)
+// and long or few rows (32 warps per row, warp k = slot k).
 constexpr int kMergeSlots = 32;
 
-struct MergeState {
-  float m, l;
-  float4 o;
-};
-
-// One of the two weights is e^0 = 1 exactly, so only the other is taken
-// from ex2; the rounding steps are those of the formula above.
-__device__ __forceinline__ void merge_into(MergeState& st, float m2, float l2, float4 o2) {
-  const float mn = fmaxf(st.m, m2);
-  float a = 1.0f, w = 1.0f;
-  if (st.m < m2) a = merge_weight(st.m, mn);
-  else w = merge_weight(m2, mn);
-  st.l = __fmaf_rn(l2, w, __fmul_rn(st.l, a));
-  st.o.x = __fmaf_rn(o2.x, w, __fmul_rn(st.o.x, a));
-  st.o.y = __fmaf_rn(o2.y, w, __fmul_rn(st.o.y, a));
-  st.o.z = __fmaf_rn(o2.z, w, __fmul_rn(st.o.z, a));
-  st.o.w = __fmaf_rn(o2.w, w, __fmul_rn(st.o.w, a));
-  st.m = mn;
-}
-
-// WPR warps per row (1 or kMergeWarps); lane l covers channels 4l .. 4l+3.
-// Grid (rows of one sequence / rows per CTA, B): blockIdx.y is the sequence.
 template <int WPR>
-__global__ void __launch_bounds__(kMergeWarps * 32, WPR == 1 ? 3 : 1)
+__global__ void __launch_bounds__(WPR == 1 ? 256 : 32 * WPR, WPR == 1 ? 4 : 1)
 merge_windows_kernel(const DecodeParams p) {
-  constexpr int kSlotsPerWarp = kMergeSlots / WPR;
-  __shared__ float sm_m[WPR == 1 ? 1 : kMergeSlots], sm_l[WPR == 1 ? 1 : kMergeSlots];
+  constexpr int kRowsPerCta = WPR == 1 ? 8 : 1;
+  __shared__ float sm_red[WPR == 1 ? 1 : kMergeSlots];
+  __shared__ float sm_l[WPR == 1 ? 1 : kMergeSlots];
   __shared__ float4 sm_o[WPR == 1 ? 1 : kMergeSlots][32];
   griddep_wait();                                 // every partial is in place
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = p.R, gq = p.g;
   const int b = blockIdx.y;
-  const int row = WPR == 1 ? (int)blockIdx.x * kMergeWarps + warp : (int)blockIdx.x;   // kh * R + r
+  const int row = WPR == 1 ? (int)blockIdx.x * kRowsPerCta + warp : (int)blockIdx.x;   // kh * R + r
   if (row >= p.Hkv * R) return;
   const int kh = row / R, r = row - kh * R;
   const int64_t rs = p.row_start[b];
@@ -1002,73 +991,83 @@ merge_windows_kernel(const DecodeParams p) {
   const float* mcol = base + (size_t)R * kD + r;
   const float* lcol = mcol + R;
   const float* ocol = base + (size_t)r * kD + 4 * lane;
-  auto load = [&](int s, float& m2, float& l2, float4& o2) {
-    const size_t off = (size_t)s * sstride;
-    m2 = __ldcg(mcol + off);
-    l2 = __ldcg(lcol + off);
-    o2 = __ldcg(reinterpret_cast<const float4*>(ocol + off));
+  auto ldo = [&](int s) { return __ldcg(reinterpret_cast<const float4*>(ocol + (size_t)s * sstride)); };
+  auto fma4 = [](float w, float4 v, float4 acc) {
+    return make_float4(__fmaf_rn(w, v.x, acc.x), __fmaf_rn(w, v.y, acc.y), __fmaf_rn(w, v.z, acc.z),
+                       __fmaf_rn(w, v.w, acc.w));
+  };
+  auto mul4 = [](float w, float4 v) {
+    return make_float4(__fmul_rn(w, v.x), __fmul_rn(w, v.y), __fmul_rn(w, v.z), __fmul_rn(w, v.w));
+  };
+  auto add4 = [](float4 a, float4 v) {
+    return make_float4(__fadd_rn(a.x, v.x), __fadd_rn(a.y, v.y), __fadd_rn(a.z, v.z), __fadd_rn(a.w, v.w));
   };
 
-  MergeState fin{-INFINITY, 0.0f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  float4 O;
+  float L;
   if constexpr (WPR == 1) {
-    // ns <= 64: slot k holds window k and, when k + 32 < ns, window k + 32.
-    // A batch of slots has all its loads in flight before it is folded.
-    constexpr int kBatch = 4;
+    // lane k: windows k and k + 32 (ns <= 64)
+    const bool h0 = lane < ns, h1 = lane + kMergeSlots < ns;
+    const float m0 = h0 ? __ldcg(mcol + (size_t)lane * sstride) : -INFINITY;
+    const float m1 = h1 ? __ldcg(mcol + (size_t)(lane + kMergeSlots) * sstride) : -INFINITY;
+    const float l0 = h0 ? __ldcg(lcol + (size_t)lane * sstride) : 0.0f;
+    const float l1 = h1 ? __ldcg(lcol + (size_t)(lane + kMergeSlots) * sstride) : 0.0f;
+    const float M = warp_max(fmaxf(m0, m1));
+    const float w0 = h0 ? exp_diff(m0, M) : 0.0f, w1 = h1 ? exp_diff(m1, M) : 0.0f;
+    L = warp_sum(h1 ? __fmaf_rn(w1, l1, __fmul_rn(w0, l0)) : __fmul_rn(w0, l0));
     const int nk = min(ns, kMergeSlots);
+    O = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kBatch = 4;                     // slots whose loads are in flight together
     for (int k0 = 0; k0 < nk; k0 += kBatch) {
-      float m1[kBatch], l1[kBatch], m2[kBatch], l2[kBatch];
-      float4 o1[kBatch], o2[kBatch];
+      float4 a[kBatch], c[kBatch];
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
-        if (k0 + i < nk) load(k0 + i, m1[i], l1[i], o1[i]);
-        if (k0 + i + kMergeSlots < ns) load(k0 + i + kMergeSlots, m2[i], l2[i], o2[i]);
+        if (k0 + i < nk) a[i] = ldo(k0 + i);
+        if (k0 + i + kMergeSlots < ns) c[i] = ldo(k0 + i + kMergeSlots);
       }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
-        if (k0 + i < nk) {
-          MergeState st{m1[i], l1[i], o1[i]};     // = the empty state merged with it
-          if (k0 + i + kMergeSlots < ns) merge_into(st, m2[i], l2[i], o2[i]);
-          if (k0 + i == 0) fin = st;
-          else merge_into(fin, st.m, st.l, st.o);
+        const int k = k0 + i;
+        if (k < nk) {
+          float4 in = mul4(__shfl_sync(0xffffffffu, w0, k), a[i]);
+          if (k + kMergeSlots < ns) in = fma4(__shfl_sync(0xffffffffu, w1, k), c[i], in);
+          O = k == 0 ? in : add4(O, in);
         }
       }
     }
   } else {
-    // this warp's slots k = warp * kSlotsPerWarp + i, each folding s = k, k + 32, ...
-    MergeState st[kSlotsPerWarp];
-#pragma unroll
-    for (int i = 0; i < kSlotsPerWarp; ++i) st[i] = MergeState{-INFINITY, 0.0f, make_float4(0.f, 0.f, 0.f, 0.f)};
-    for (int s0 = 0; s0 < ns; s0 += kMergeSlots) {
-#pragma unroll
-      for (int i = 0; i < kSlotsPerWarp; ++i) {
-        const int s = s0 + warp * kSlotsPerWarp + i;
-        if (s < ns) {
-          float m2, l2;
-          float4 o2;
-          load(s, m2, l2, o2);
-          if (s0 == 0) st[i] = MergeState{m2, l2, o2};   // = the empty state merged with it
-          else merge_into(st[i], m2, l2, o2);
-        }
+    // warp k = slot k: windows k, k + 32, ...
+    float mloc = -INFINITY;
+    for (int s = warp; s < ns; s += kMergeSlots) mloc = fmaxf(mloc, __ldcg(mcol + (size_t)s * sstride));
+    if (lane == 0) sm_red[warp] = mloc;
+    __syncthreads();
+    const float M = warp_max(sm_red[lane]);     // the 32 slot maxima (-inf for empty slots)
+    float4 in = make_float4(0.f, 0.f, 0.f, 0.f);
+    float il = 0.0f;
+#pragma unroll 4
+    for (int s = warp; s < ns; s += kMergeSlots) {
+      const float w = exp_diff(__ldcg(mcol + (size_t)s * sstride), M);
+      const float ls = __ldcg(lcol + (size_t)s * sstride);
+      const float4 v = ldo(s);
+      if (s == warp) {
+        in = mul4(w, v);
+        il = __fmul_rn(w, ls);
+      } else {
+        in = fma4(w, v, in);
+        il = __fmaf_rn(w, ls, il);
       }
     }
-#pragma unroll
-    for (int i = 0; i < kSlotsPerWarp; ++i) {
-      const int k = warp * kSlotsPerWarp + i;
-      if (lane == 0) {
-        sm_m[k] = st[i].m;
-        sm_l[k] = st[i].l;
-      }
-      sm_o[k][lane] = st[i].o;
-    }
+    sm_o[warp][lane] = in;
+    if (lane == 0) sm_l[warp] = il;
     __syncthreads();
     if (warp != 0) return;
-    fin = MergeState{sm_m[0], sm_l[0], sm_o[0][lane]};
-    for (int k = 1; k < kMergeSlots && k < ns; ++k) merge_into(fin, sm_m[k], sm_l[k], sm_o[k][lane]);
+    L = warp_sum(sm_l[lane]);                   // empty slots hold 0
+    O = sm_o[0][lane];
+    for (int k = 1; k < kMergeSlots && k < ns; ++k) O = add4(O, sm_o[k][lane]);
   }
   const int j = r / gq, h = kh * gq + (r - j * gq);
   float4* dst = reinterpret_cast<float4*>(p.out + ((((int64_t)b * p.M + j) * p.Hq + h) * kD)) + lane;
-  *dst = make_float4(__fdiv_rn(fin.o.x, fin.l), __fdiv_rn(fin.o.y, fin.l), __fdiv_rn(fin.o.z, fin.l),
-                     __fdiv_rn(fin.o.w, fin.l));
+  *dst = make_float4(__fdiv_rn(O.x, L), __fdiv_rn(O.y, L), __fdiv_rn(O.z, L), __fdiv_rn(O.w, L));
 }
 
 // ------------------------------------------------------------------- host
@@ -1182,15 +1181,14 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
   else if (p.R <= 32) e = launch_rows<4, 1>(p, maps, stream);
   else e = launch_rows<4, 2>(p, maps, stream);
   if (e != cudaSuccess || p.nsplit_max <= 1) return e;
-  // 3. the window merge: one warp per row while no row has more than 64
-  //    windows, else eight warps per row (the same arithmetic either way)
+  // 3. the window merge: one warp per row when rows are many and no row has
+  //    more than 64 windows, else 32 warps per row (the same arithmetic)
   const int rows_b = p.Hkv * p.R;                 // rows of one sequence
-  if (p.nsplit_max <= 2 * kMergeSlots)
-    return launch_pdl(merge_windows_kernel<1>,
-                      dim3((unsigned)((rows_b + kMergeWarps - 1) / kMergeWarps), (unsigned)p.B),
-                      dim3(kMergeWarps * 32), 0, stream, p);
-  return launch_pdl(merge_windows_kernel<kMergeWarps>, dim3((unsigned)rows_b, (unsigned)p.B),
-                    dim3(kMergeWarps * 32), 0, stream, p);
+  if (p.nsplit_max <= 2 * kMergeSlots && (int64_t)rows_b * p.B >= 4096)
+    return launch_pdl(merge_windows_kernel<1>, dim3((unsigned)((rows_b + 7) / 8), (unsigned)p.B),
+                      dim3(256), 0, stream, p);
+  return launch_pdl(merge_windows_kernel<kMergeSlots>, dim3((unsigned)rows_b, (unsigned)p.B),
+                    dim3(32 * kMergeSlots), 0, stream, p);
 }
 
 }  // namespace kattn
