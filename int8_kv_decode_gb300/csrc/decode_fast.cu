@@ -48,6 +48,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <atomic>
 
 #include "device_common.cuh"
@@ -79,11 +80,12 @@ struct __align__(1024) SmemT {
   static constexpr int kRows = NG * NR * 8;                  // query rows of the CTA (rpad)
   static constexpr int kF = (KATTN_QK_INT8 && NR == 1) ? 1 : 0;   // no f16 fragments
 
-  uint8_t ring[NG * kSpansPerCta][kRing][2][kBlockBytes];    // per warp: [stage][K|V]
+  uint8_t ring[kSpansPerCta][kRing][2][kBlockBytes];         // per span: [stage][K|V]
   float slot[NG][2][NR * 8 * kD];                            // span merge, fragment order
   uint8_t qbuf[kRows * (kD + 4)];                            // item's int8 rows, then scales
   uint2 qfrag[kF ? 1 : NG][kF ? 1 : NR][kF ? 1 : 8][kF ? 1 : 32];   // f16 query fragments
-  uint64_t full[NG * kSpansPerCta][kRing];
+  uint64_t full[kSpansPerCta][kRing];                        // the stage's copy landed
+  uint64_t empty[kSpansPerCta][kRing];                       // NG > 1: every group read it
   uint64_t qbar;
   float wm[NG][kSpansPerCta][NR * 8];                        // per-span running max
   float wl[NG][kSpansPerCta][NR * 8];                        // per-span row sum
@@ -93,6 +95,10 @@ struct __align__(1024) SmemT {
 // ------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -383,23 +389,46 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodePa
   }
 }
 
-// One thread per work item (grid-stride): b by binary search over prefix.
+// The work items, one per thread: a warp takes 32 consecutive items.  A
+// 32-way search over prefix (every lane probes one entry per round) finds
+// the sequence b0 of the warp's first item; the 32 items span at most 32
+// sequences, so one more load of prefix[b0 + 1 .. b0 + 32] places each lane.
 constexpr int kListThreads = 256;
 
 __global__ void __launch_bounds__(kListThreads) list_kernel(const DecodeParams p) {
   griddep_wait();                                 // prefix and the count
   griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
   const int total = (int)__ldcg(p.item_count);
-  for (int j = blockIdx.x * kListThreads + threadIdx.x; j < total; j += gridDim.x * kListThreads) {
-    int lo = 0, hi = p.B;                         // prefix[lo] <= j < prefix[hi]
+  const int warps = gridDim.x * (kListThreads / 32);
+  for (int j0 = (blockIdx.x * (kListThreads / 32) + (threadIdx.x >> 5)) * 32; j0 < total;
+       j0 += warps * 32) {
+    int lo = 0, hi = p.B, base = 0;               // prefix[lo] = base <= j0 < prefix[hi]
     while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldcg(p.prefix + mid) <= j) lo = mid;
-      else hi = mid;
+      const int step = (hi - lo + 31) >> 5;
+      const int idx = lo + step * lane;
+      const int v = (lane > 0 && idx < hi) ? __ldcg(p.prefix + idx) : base;
+      const bool ok = lane == 0 || (idx < hi && v <= j0);
+      const int last = 31 - __clz(__ballot_sync(0xffffffffu, ok));
+      base = __shfl_sync(0xffffffffu, v, last);
+      lo += step * last;
+      hi = min(hi, lo + step);
     }
-    const int i = j - __ldcg(p.prefix + lo), w = i / p.Hkv, kh = i - w * p.Hkv;
-    p.items[j] = make_int4(lo | (kh << 16), w, kh * p.cap_rows + (int)p.row_start[lo],
-                           p.ctx_len[lo]);
+    // boundary i = prefix[lo + 1 + i]: the first item of sequence lo + 1 + i
+    const int bi = lo + 1 + lane;
+    const int bound = bi <= p.B ? __ldcg(p.prefix + bi) : INT_MAX;
+    const int j = j0 + lane;
+    int crossed = 0;                              // boundaries at or before item j
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) crossed += __shfl_sync(0xffffffffu, bound, i) <= j;
+    const int b = lo + crossed;
+    const int prev = __shfl_sync(0xffffffffu, bound, max(crossed - 1, 0));   // every lane shuffles
+    const int first = crossed == 0 ? base : prev;
+    if (j < total) {
+      const int i = j - first, w = i / p.Hkv, kh = i - w * p.Hkv;
+      p.items[j] = make_int4(b | (kh << 16), w, kh * p.cap_rows + (int)p.row_start[b],
+                             p.ctx_len[b]);
+    }
   }
 }
 
@@ -431,7 +460,11 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   const int g = lane >> 2, c = lane & 3;
   const int gq = p.g, M = p.M, R = p.R;
   const int row0 = grp * RG;
-  uint64_t* full = sm.full[warp];
+  // Span kw's ring is filled by warp kw of group 0 and read by warp kw of
+  // every group (the groups hold different query rows).
+  uint64_t* full = sm.full[kw];
+  uint64_t* empty = sm.empty[kw];
+  const bool producer = grp == 0;
   // Per thread and fixed for the launch: the draft column j of rows
   // 8nr + 2c + e of the group, and where those rows sit in out (head kh * g
   // + r % g; add kh * g * d and the sequence's offset).
@@ -445,8 +478,13 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
       orow[nr][e] = ((r / gq) * p.Hq + r % gq) * kD + 16 * g;
     }
 
+  if (lane == 0 && producer) {
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NG);
+    }
+  }
   if (lane == 0) {
-    for (int s = 0; s < kRing; ++s) mbar_init(&full[s], 1);
     if (warp == 0) mbar_init(&sm.qbar, 1);
     sm.fail[warp] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -475,16 +513,27 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   // cursor runs over this item's blocks, then the next item's.
   Span psp = span_of(it0, kw, M);
   int pitem = 0, pblk = 0, ist = 0, inflight = 0;
+  uint32_t used = 0, eph = 0;                     // NG > 1: stages filled before; empty parities
   const uint64_t kv_policy = l2_evict_first();
-  auto produce = [&]() {
+  // Returns false if a stage was never released (a bounded wait ran out).
+  auto produce = [&]() -> bool {
+    if (!producer) return true;
     while (inflight < kRing) {
       if (pblk < psp.nb) {
+        if constexpr (NG > 1) {
+          if ((used >> ist) & 1u) {               // wait until every group has read it
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[ist], (eph >> ist) & 1u)))
+              return false;
+            eph ^= 1u << ist;
+          }
+          used |= 1u << ist;
+        }
         if (lane == 0) {
           asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
           mbar_expect_tx(&full[ist], 2 * kBlockBytes);
           const int row = psp.row + pblk * kBlockBk;
-          tma_load_block(sm.ring[warp][ist][0], &maps.k, row, &full[ist], kv_policy);
-          tma_load_block(sm.ring[warp][ist][1], &maps.v, row, &full[ist], kv_policy);
+          tma_load_block(sm.ring[kw][ist][0], &maps.k, row, &full[ist], kv_policy);
+          tma_load_block(sm.ring[kw][ist][1], &maps.v, row, &full[ist], kv_policy);
         }
         ++pblk;
         ++inflight;
@@ -497,8 +546,9 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
         break;
       }
     }
+    return true;
   };
-  produce();
+  bool prod_ok = produce();
 
   // ---- consumer state
   Span sp = span_of(it0, kw, M);
@@ -607,7 +657,8 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) o[md][nr][u] = 0.0f;
 
-    bool failed = !q_ok;
+    bool failed = !q_ok || !prod_ok;
+    prod_ok = true;
     const int nb = q_ok ? sp.nb : 0;
     for (int i = 0; i < nb; ++i) {
       const int t0 = sp.s0 + i * kBlockBk;
@@ -626,8 +677,8 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
         failed = true;
         break;
       }
-      const uint8_t* Kt = sm.ring[warp][cst][0];
-      const uint8_t* Vt = sm.ring[warp][cst][1];
+      const uint8_t* Kt = sm.ring[kw][cst][0];
+      const uint8_t* Vt = sm.ring[kw][cst][1];
       // ---- QK for both 16-key halves hf.  sc[hf][nr]: [0] key 16hf+g row 2c,
       // [1] key 16hf+g row 2c+1, [2] key 16hf+g+8 row 2c, [3] key 16hf+g+8 row
       // 2c+1 (rows inside n-tile nr).
@@ -794,12 +845,18 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
       }
 
       __syncwarp();
-      --inflight;
+      if constexpr (NG > 1) {
+        if (lane == 0) mbar_arrive(&empty[cst]);  // this group is done with the stage
+      }
+      if (producer) --inflight;
       if (++cst == kRing) {
         cst = 0;
         cph ^= 1u;
       }
-      produce();                                  // refill the stage just read
+      if (!produce()) {                           // refill the stage just read
+        failed = true;
+        break;
+      }
     }
 
     // ---- per-span row sums and maxima
@@ -948,7 +1005,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
       psp = sp;                                   // it had nothing left to read ahead
       pblk = 0;
     }
-    produce();
+    prod_ok = produce();
   }
 }
 
@@ -1171,14 +1228,15 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t max_items = (int64_t)p.B * p.nsplit_max * p.Hkv;
-  const int list_blocks = (int)std::min<int64_t>((max_items + kListThreads - 1) / kListThreads, 4096);
+  const int list_blocks = (int)std::min<int64_t>((max_items + kListThreads - 1) / kListThreads, 1024);
   if ((e = launch_pdl(list_kernel, dim3((unsigned)list_blocks), dim3(kListThreads), 0, stream, p)) !=
       cudaSuccess)
     return e;
   // 2. the split-KV pass
   if (p.R <= 8) e = launch_rows<1, 1>(p, maps, stream);
   else if (p.R <= 16) e = launch_rows<2, 1>(p, maps, stream);
-  else if (p.R <= 32) e = launch_rows<4, 1>(p, maps, stream);
+  else if (p.R <= 32) e = launch_rows<2, 2>(p, maps, stream);
+  else if (p.R <= 48) e = launch_rows<3, 2>(p, maps, stream);
   else e = launch_rows<4, 2>(p, maps, stream);
   if (e != cudaSuccess || p.nsplit_max <= 1) return e;
   // 3. the window merge: one warp per row when rows are many and no row has

@@ -45,7 +45,9 @@ struct WorkspaceLayout {
 __host__ __device__ inline int nsplit_for(int keys) { return (keys + kSplitC - 1) / kSplitC; }
 
 // Query rows a decode CTA holds: R rounded up to the row tile of its variant.
-__host__ __device__ inline int row_tile(int R) { return R <= 8 ? 8 : R <= 16 ? 16 : R <= 32 ? 32 : 64; }
+__host__ __device__ inline int row_tile(int R) {
+  return R <= 8 ? 8 : R <= 16 ? 16 : R <= 32 ? 32 : R <= 48 ? 48 : 64;
+}
 __host__ __device__ inline int qpack_bytes(int rpad) { return rpad * (kD + 4); }
 __host__ __device__ inline int partial_stride(int R) { return R * kD + ((2 * R + 3) / 4) * 4; }
 
