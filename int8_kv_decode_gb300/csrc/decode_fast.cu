@@ -1239,10 +1239,22 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
   else if (p.R <= 48) e = launch_rows<3, 2>(p, maps, stream);
   else e = launch_rows<4, 2>(p, maps, stream);
   if (e != cudaSuccess || p.nsplit_max <= 1) return e;
-  // 3. the window merge: one warp per row when rows are many and no row has
-  //    more than 64 windows, else 32 warps per row (the same arithmetic)
+  // 3. the window merge (the same arithmetic in both shapes).  Estimated
+  //    time = waves x dependent loads per row: one warp per row (32 rows
+  //    per SM at once; a load round per 4 windows) or 32 warps per row (one
+  //    row per SM; a round per 128 windows), for rows of up to 64 windows.
   const int rows_b = p.Hkv * p.R;                 // rows of one sequence
-  if (p.nsplit_max <= 2 * kMergeSlots && (int64_t)rows_b * p.B >= 4096)
+  const int64_t all_rows = (int64_t)rows_b * p.B;
+  int sms = 0;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      sms = 1;
+  }
+  const int64_t est_warp = (all_rows + 32LL * sms - 1) / (32LL * sms) * ((p.nsplit_max + 3) / 4 + 2);
+  const int64_t est_cta = (all_rows + sms - 1) / sms * ((p.nsplit_max + 127) / 128 + 3);
+  if (p.nsplit_max <= 2 * kMergeSlots && est_warp <= est_cta)
     return launch_pdl(merge_windows_kernel<1>, dim3((unsigned)((rows_b + 7) / 8), (unsigned)p.B),
                       dim3(256), 0, stream, p);
   return launch_pdl(merge_windows_kernel<kMergeSlots>, dim3((unsigned)rows_b, (unsigned)p.B),
