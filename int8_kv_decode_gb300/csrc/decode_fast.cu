@@ -87,8 +87,12 @@ struct __align__(1024) SmemT {
   uint64_t full[kSpansPerCta][kRing];                        // the stage's copy landed
   uint64_t empty[kSpansPerCta][kRing];                       // NG > 1: every group read it
   uint64_t qbar;
-  float wm[NG][kSpansPerCta][NR * 8];                        // per-span running max
-  float wl[NG][kSpansPerCta][NR * 8];                        // per-span row sum
+  // Per-span running max and row sum, double-buffered by item parity: warp 0
+  // reads an item's values after the other warps have moved on to the next
+  // item; a buffer comes back two items later, after a CTA barrier that
+  // warp 0 reaches only once it is done reading.
+  float wm[2][NG][kSpansPerCta][NR * 8];
+  float wl[2][NG][kSpansPerCta][NR * 8];
   int fail[NG * kSpansPerCta];                               // per warp: a copy never arrived
 };
 
@@ -322,6 +326,8 @@ __device__ __forceinline__ void load_span_scales(const DecodeParams& p, const It
 // row r < R is query (column j = r / g, head kh * g + r % g) quantized per
 // row, rows r >= R are zero.  The last block writes the work-item prefix.
 constexpr int kPrepWarps = 4;
+constexpr int kFusedListMaxB = 2048;              // prepare writes the list itself up to here
+constexpr int kListPerBlock = 1024;               // items per list block of prepare
 
 __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodeParams p,
                                                                   int q_blocks) {
@@ -351,12 +357,16 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodePa
     if (lane == 0) reinterpret_cast<float*>(pack + p.rpad * kD)[r] = s;
     return;
   }
-  // The last block: prefix[b] = work items (windows x kv heads) of the valid
-  // sequences before b.  Thread i takes a run of consecutive sequences,
-  // counts them, the runs are scanned across the block, and each thread
-  // writes its run.
+  // prefix[b] = work items (windows x kv heads) of the valid sequences
+  // before b.  Thread i takes a run of consecutive sequences, counts them,
+  // the runs are scanned across the block, and each thread writes its run --
+  // into shared memory (a list block: B <= kFusedListMaxB) or global memory
+  // (the one prefix block for list_kernel).
   constexpr int kThreads = kPrepWarps * 32;
   __shared__ int s_warp[kPrepWarps];
+  __shared__ int s_pre[kFusedListMaxB + 1];
+  const bool fused = p.list_blocks > 0;
+  int* pre = fused ? s_pre : p.prefix;
   auto items_of = [&](int b) -> int {
     const int64_t rs = p.row_start[b];
     const int ctx = p.ctx_len[b];
@@ -380,12 +390,29 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodePa
   for (int w = 0; w < kPrepWarps; ++w)
     if (w < warp) base += s_warp[w];
   for (int b = b_lo; b < b_hi; ++b) {
-    p.prefix[b] = base;
+    pre[b] = base;
     base += items_of(b);
   }
   if (tid == kThreads - 1) {                      // its run ends at B
-    p.prefix[p.B] = base;
-    *p.item_count = (uint32_t)base;
+    pre[p.B] = base;
+    if (!fused || blockIdx.x == (unsigned)q_blocks) *p.item_count = (uint32_t)base;
+  }
+  if (!fused) return;
+  // List block k writes items j = k * kThreads + tid, stepping by all list
+  // blocks' threads: a thread finds its item's sequence by binary search in
+  // the shared prefix.
+  __syncthreads();
+  const int total = s_pre[p.B];
+  for (int j = ((int)blockIdx.x - q_blocks) * kThreads + tid; j < total; j += p.list_blocks * kThreads) {
+    int lo = 0, hi = p.B;                         // s_pre[lo] <= j < s_pre[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pre[mid] <= j) lo = mid;
+      else hi = mid;
+    }
+    const int i = j - s_pre[lo], w = i / p.Hkv, kh = i - w * p.Hkv;
+    p.items[j] = make_int4(lo | (kh << 16), w, kh * p.cap_rows + (int)p.row_start[lo],
+                           p.ctx_len[lo]);
   }
 }
 
@@ -557,6 +584,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   load_span_scales(p, it1, span_of(it1, kw, M), lane, ksn, vsn);
   int cst = 0;                                    // ring stage of the next block to consume
   uint32_t cph = 0, qph = 0;                      // its mbarrier parity; the query barrier's
+  int par = 0;                                    // item parity: the (m, l) buffer
 
   for (;;) {
     // ---- the item's queries (packed by prepare_kernel)
@@ -869,8 +897,8 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
         v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 8));
         v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 16));
         if (g == 0) {
-          sm.wl[grp][kw][nr * 8 + 2 * c + e] = v;
-          sm.wm[grp][kw][nr * 8 + 2 * c + e] = m_run[nr][e];
+          sm.wl[par][grp][kw][nr * 8 + 2 * c + e] = v;
+          sm.wm[par][grp][kw][nr * 8 + 2 * c + e] = m_run[nr][e];
         }
       }
     if (lane == 0 && failed) sm.fail[warp] = 1;
@@ -912,11 +940,11 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int rr = nr * 8 + 2 * c + e;
-        float m = sm.wm[grp][0][rr];
+        float m = sm.wm[par][grp][0][rr];
 #pragma unroll
-        for (int w = 1; w < kSpansPerCta; ++w) m = fmaxf(m, sm.wm[grp][w][rr]);
+        for (int w = 1; w < kSpansPerCta; ++w) m = fmaxf(m, sm.wm[par][grp][w][rr]);
         mwin[nr][e] = m;
-        wt[nr][e] = __fmul_rn(merge_weight(sm.wm[grp][kw][rr], m), down_row[nr][e]);
+        wt[nr][e] = __fmul_rn(merge_weight(sm.wm[par][grp][kw][rr], m), down_row[nr][e]);
       }
     const int bar_pair = 1 + 2 * grp, bar_even = 2 + 2 * grp;
     float* slot = sm.slot[grp][kw >> 1];
@@ -964,7 +992,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
             float l = 0.0f;                       // window row sum, spans in order
 #pragma unroll
             for (int w = 0; w < kSpansPerCta; ++w)
-              l = __fmaf_rn(sm.wl[grp][w][rr], merge_weight(sm.wm[grp][w][rr], mwin[nr][e]), l);
+              l = __fmaf_rn(sm.wl[par][grp][w][rr], merge_weight(sm.wm[par][grp][w][rr], mwin[nr][e]), l);
             if (whole) {
               float* dst = p.out + ((int64_t)b * M * p.Hq + kh * gq) * kD + orow[nr][e];
 #pragma unroll
@@ -999,6 +1027,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     }
     load_span_scales(p, it1, span_of(it1, kw, M), lane, ksn, vsn);
     qph ^= 1u;
+    par ^= 1;
     if (pitem == 1) {
       pitem = 0;                                  // the producer is already on this item
     } else {
@@ -1224,14 +1253,25 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
   //    caller's q, row_start and ctx_len)
   const int64_t qrows = (int64_t)p.B * p.Hkv * p.rpad;
   const int q_blocks = (int)((qrows + kPrepWarps - 1) / kPrepWarps);
-  prepare_kernel<<<q_blocks + 1, kPrepWarps * 32, 0, stream>>>(p, q_blocks);
+  //    Up to kFusedListMaxB sequences its list blocks also write the work
+  //    items; beyond, one block writes the prefix and list_kernel the items.
+  const int64_t max_items = (int64_t)p.B * p.nsplit_max * p.Hkv;
+  DecodeParams pp = p;
+  pp.list_blocks =
+      p.B <= kFusedListMaxB
+          ? (int)std::min<int64_t>((max_items + kListPerBlock - 1) / kListPerBlock, 256)
+          : 0;
+  prepare_kernel<<<q_blocks + (pp.list_blocks > 0 ? pp.list_blocks : 1), kPrepWarps * 32, 0, stream>>>(
+      pp, q_blocks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t max_items = (int64_t)p.B * p.nsplit_max * p.Hkv;
-  const int list_blocks = (int)std::min<int64_t>((max_items + kListThreads - 1) / kListThreads, 1024);
-  if ((e = launch_pdl(list_kernel, dim3((unsigned)list_blocks), dim3(kListThreads), 0, stream, p)) !=
-      cudaSuccess)
-    return e;
+  if (pp.list_blocks == 0) {
+    const int list_blocks =
+        (int)std::min<int64_t>((max_items + kListThreads - 1) / kListThreads, 1024);
+    if ((e = launch_pdl(list_kernel, dim3((unsigned)list_blocks), dim3(kListThreads), 0, stream,
+                        p)) != cudaSuccess)
+      return e;
+  }
   // 2. the split-KV pass
   if (p.R <= 8) e = launch_rows<1, 1>(p, maps, stream);
   else if (p.R <= 16) e = launch_rows<2, 1>(p, maps, stream);

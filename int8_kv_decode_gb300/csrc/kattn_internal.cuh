@@ -86,6 +86,7 @@ struct DecodeParams {
   float* partials;
   int B, M, Hq, Hkv, g, R;
   int rpad;             // row_tile(R)
+  int list_blocks;      // > 0: prepare_kernel writes the work items in this many blocks
   int cap_rows, max_ctx, nsplit_max;
   float sm_scale;       // already resolved (never 0)
   int p_mode;

@@ -226,6 +226,25 @@ def test_odd_row_count_over_several_windows(g, M):
         assert np.array_equal(bits(got[:, j:j + 1]), bits(one))
 
 
+@pytest.mark.parametrize("B", [1000, 2100])
+def test_many_short_sequences(B):
+    # Many short sequences: most work items are one short window, so warps
+    # of a CTA reach the next item at very different times.  Above 2048
+    # sequences the work list is written by its own kernel rather than by
+    # the query-packing launch.  Sampled rows against the oracle, and the
+    # bytes of each half of the batch decoded alone.
+    import int8_kv_decode_gb300 as K
+    wl = custom(f"many{B}", B, 1, 8, 2, ("uniform", 1, 1200), outliers=False)
+    c = upload(wl)
+    got = run(c).cpu().numpy()
+    rows = sample_rows(c.x, 40, seed=3)
+    assert_f32_tolerance(got, oracle_decode(c, rows=rows), row_mask(got.shape, rows))
+    for lo, hi in ((0, B // 2), (B // 2, B)):
+        half = K.decode(c.q[lo:hi].contiguous(), c.k8, c.ks, c.v8, c.vs, c.rs[lo:hi].contiguous(),
+                        c.ctx[lo:hi].contiguous(), int(c.x.ctx[lo:hi].max())).cpu().numpy()
+        assert np.array_equal(bits(got[lo:hi]), bits(half)), (lo, hi)
+
+
 def test_decode_replays_in_a_cuda_graph():
     # The three launches of a fast decode, captured once and replayed, give
     # the bytes of an ordinary call.
