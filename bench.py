@@ -219,16 +219,17 @@ def time_oracle(wl, budget_s: float, max_seq: int = 12):
     spent = 0.0
     nbytes = nq = n = 0
     with limit:
-        for b in range(x.wl.B):
-            t0 = time.perf_counter()
-            oracle.attention.decode(x.q[b:b + 1], k8, ks, v8, vs, x.row_start[b:b + 1],
-                                    x.ctx[b:b + 1])
-            spent += time.perf_counter() - t0
-            nbytes += kv_bytes(x.ctx[b:b + 1], wl.M, wl.Hkv)
-            nq += wl.M
-            n += 1
-            if spent >= budget_s:
-                break
+        while spent < budget_s:                   # passes over the sample until the budget
+            for b in range(x.wl.B):
+                t0 = time.perf_counter()
+                oracle.attention.decode(x.q[b:b + 1], k8, ks, v8, vs, x.row_start[b:b + 1],
+                                        x.ctx[b:b + 1])
+                spent += time.perf_counter() - t0
+                nbytes += kv_bytes(x.ctx[b:b + 1], wl.M, wl.Hkv)
+                nq += wl.M
+                n += 1
+                if spent >= budget_s:
+                    break
     return nbytes / spent / 1e9, nq / spent, spent, n, 1
 
 
@@ -463,8 +464,9 @@ def run_ours(args):
     if world == 1 and not args.no_cpu_baseline:
         gbs, qps, secs, nseq, cores = time_oracle(wl, args.cpu_budget)
         cpu = {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": (f"{nseq} whole sequences of {wl.name} ({secs:.1f} s single-threaded, "
-                          f"float64 reference, f32 P); GB/s = their KV bytes / time"),
+               "sample": (f"{nseq} sequence decodes ({secs:.1f} s single-threaded) over repeated "
+                          f"passes on 12 whole sequences of {wl.name}, float64 reference, f32 P; "
+                          f"GB/s = their KV bytes / time"),
                "queries_per_s": qps}
 
     line = {
