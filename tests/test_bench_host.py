@@ -85,3 +85,10 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_all_cores_oracle_baseline_runs_in_spawned_processes():
+    import bench
+    from synth import WORKLOADS
+    gbs, cores, secs = bench.time_oracle_all_cores(WORKLOADS["tiny"], 0.2)
+    assert cores >= 1 and secs >= 0.2 and gbs > 0
