@@ -244,7 +244,8 @@ def _oracle_worker(job):
     import dataclasses
     wl = WORKLOADS[wl_name]
     rng = np.random.Generator(np.random.PCG64(wl.index * 1000))
-    ctx = make_lengths(wl, rng)[i:i + 1]
+    lengths = make_lengths(wl, rng)
+    ctx = lengths[i % len(lengths):][:1]
     x = make_workload(dataclasses.replace(wl, B=1), rep=100 + i, ctx_override=ctx)
     k8, ks = oracle.quant.quantize_kv(x.k_rows)
     v8, vs = oracle.quant.quantize_kv(x.v_rows)
