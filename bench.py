@@ -2,8 +2,8 @@
 """Decode-attention benchmark: KV GB/s and queries/s on GB300, % of HBM roofline.
 
 One step = one decode step of the hot path over one batch of synthetic
-sequences: quantize this step's appended K and V rows into the int8 cache
-(one scatter launch each) and run kattn_decode over every sequence.  The
+sequences: kattn_decode_append quantizes this step's appended K and V rows
+into the int8 cache and decodes every sequence, in one call.  The
 default workload is the serving mix: 256 ragged sequences, contexts
 log-uniform in [512, 32768], 32 query / 4 KV heads, head_dim 128, M = 1,
 float32 P, fast mode.
@@ -54,11 +54,12 @@ def qo_bytes(B: int, M: int, Hq: int, d: int = HEAD_DIM) -> int:
     return 2 * B * M * Hq * d * 4
 
 
-def decode_launches(max_ctx: int, M: int) -> int:
-    """Kernels one fast-mode kattn_decode launches: query packing, the work
-    list and the split-KV pass, plus the window merge when the longest row
-    spans more than one 512-key window."""
-    return 3 + (int(max_ctx) + M - 1 > 512)
+def decode_launches(max_ctx: int, M: int, B: int) -> int:
+    """Kernels one fast-mode kattn_decode (or kattn_decode_append) launches:
+    query packing (with the append and, up to 2048 sequences, the work list),
+    the work list above 2048 sequences, the split-KV pass, and the window
+    merge when the longest row spans more than one 512-key window."""
+    return 2 + (B > 2048) + (int(max_ctx) + M - 1 > 512)
 
 
 def append_rows(row_start, ctx, M: int):
@@ -379,18 +380,15 @@ def run_ours(args):
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
 
-    def append(i):
-        k8, ks, v8, vs = caches[i % n_copies]
-        K.quantize_kv_rows(knew, dst, k8, ks)
-        K.quantize_kv_rows(vnew, dst, v8, vs)
-
     def decode(i):
         k8, ks, v8, vs = caches[i % n_copies]
         K.decode(q, k8, ks, v8, vs, rs, ctx, max_ctx, out=out, workspace=ws)
 
     def step(i):
-        append(i)
-        decode(i)
+        # this step's K/V rows appended inside the decode call
+        k8, ks, v8, vs = caches[i % n_copies]
+        K.decode_append(q, knew, vnew, dst, k8, ks, v8, vs, rs, ctx, max_ctx, out=out,
+                        workspace=ws)
 
     for i in range(args.warmup):
         step(i)
@@ -538,7 +536,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": total_bytes / e_tmax / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": (2 + decode_launches(max_ctx, M)) * args.steps,
+        "gpu_launches": decode_launches(max_ctx, M, B) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

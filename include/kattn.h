@@ -170,6 +170,24 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale,
                  int exact_mode, float* out, void* workspace,
                  size_t workspace_bytes, void* stream);
 
+/* One decode step with its KV append: kattn_quantize_kv_rows of k_new into
+ * (k, k_scale) and of v_new into (v, v_scale), then kattn_decode in fast mode
+ * (exact_mode = 0), in fewer launches -- the append runs inside the decode's
+ * query-packing launch, so the decode reads the rows it has just written.
+ * k_new, v_new: float32 [n_new][Hkv][d], row r at + r*row_stride_elems;
+ * dst_rows: int64 [n_new] on the device (out-of-range rows are skipped, as in
+ * kattn_quantize_kv_rows).  For the new rows to be attended, the caller gives
+ * them cache rows inside the sequences' visible ranges (e.g. the M draft rows
+ * of each sequence, row_start[b] + ctx_len[b] - 1 + j).  The cache bytes and
+ * `out` equal those of the separate calls, byte for byte.  Other arguments,
+ * workspace and errors as kattn_decode; n_new = 0 is a plain decode. */
+int kattn_decode_append(const float* q, const float* k_new, const float* v_new,
+                        const int64_t* dst_rows, int n_new, int64_t row_stride_elems,
+                        int8_t* k, float* k_scale, int8_t* v, float* v_scale,
+                        const int64_t* row_start, const int32_t* ctx_len, int B, int M, int Hq,
+                        int Hkv, int d, int cap_rows, int max_ctx, float sm_scale, int p_mode,
+                        float* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Allocation-free form of kattn_decode in fast mode (exact_mode = 0).  The
  * pages have no counterpart to it: it exists for callers that cannot give the
  * library a workspace -- an engine whose device memory belongs to its own

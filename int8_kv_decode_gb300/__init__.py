@@ -8,6 +8,7 @@ from .api import (  # noqa: F401
     P_MODES,
     alloc_workspace,
     decode,
+    decode_append,
     decode_workspace_size,
     expf_constants,
     get_device_status,

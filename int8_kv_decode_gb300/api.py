@@ -141,6 +141,46 @@ def decode(q, k, k_scale, v, v_scale, row_start, ctx_len, max_ctx: int, *,
     return out
 
 
+def decode_append(q, k_new, v_new, dst_rows, k, k_scale, v, v_scale, row_start, ctx_len,
+                  max_ctx: int, *, out=None, p_mode=0, sm_scale: float = 0.0, workspace=None):
+    """Append rows k_new / v_new [n][Hkv][d] f32 at cache rows dst_rows [n]
+    (int64), then decode (fast mode): one call of kattn_decode_append."""
+    _need(q, torch.float32, "q", 4)
+    _need(k_new, torch.float32, "k_new", 3)
+    _need(v_new, torch.float32, "v_new", 3)
+    _need(dst_rows, torch.int64, "dst_rows", 1)
+    _need(k, torch.int8, "k", 3)
+    _need(v, torch.int8, "v", 3)
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(v_scale, torch.float32, "v_scale", 2)
+    _need(row_start, torch.int64, "row_start", 1)
+    _need(ctx_len, torch.int32, "ctx_len", 1)
+    B, M, Hq, d = q.shape
+    Hkv, cap, _ = k.shape
+    n_new = k_new.shape[0]
+    if tuple(v_new.shape) != tuple(k_new.shape) or dst_rows.numel() != n_new \
+            or k_new.shape[1] != Hkv or k_new.shape[2] != d:
+        raise ValueError("k_new / v_new / dst_rows shapes disagree with the cache")
+    if tuple(v.shape) != tuple(k.shape) or tuple(k_scale.shape) != (Hkv, cap) \
+            or tuple(v_scale.shape) != (Hkv, cap):
+        raise ValueError("k/v/scales shapes disagree")
+    mode = P_MODES.get(p_mode, p_mode) if isinstance(p_mode, str) else int(p_mode)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, torch.float32, "out", 4)
+    if workspace is None:
+        workspace = alloc_workspace(B, M, Hq, max_ctx, q.device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    lib = _lib.load()
+    _lib.check("kattn_decode_append", lib.kattn_decode_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(dst_rows), n_new, Hkv * d, _ptr(k), _ptr(k_scale),
+        _ptr(v), _ptr(v_scale), _ptr(row_start), _ptr(ctx_len), B, M, Hq, Hkv, d, cap,
+        int(max_ctx), float(sm_scale), mode, _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(q.device)))
+    return out
+
+
 def qk_scores_debug(q, k, k_scale, row_start, ctx_len, max_ctx: int, *, scores=None,
                     want_q=False):
     """Integer QK scores [B][M][Hq][max_ctx + M - 1] (int32); entries t >= L_j

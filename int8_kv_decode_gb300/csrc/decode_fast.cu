@@ -324,15 +324,32 @@ __device__ __forceinline__ void load_span_scales(const DecodeParams& p, const It
 // ------------------------------------------------------------------ prepare
 // Blocks [0, q_blocks): one warp per packed query row (b, kv head, r < rpad):
 // row r < R is query (column j = r / g, head kh * g + r % g) quantized per
-// row, rows r >= R are zero.  The last block writes the work-item prefix.
+// row, rows r >= R are zero.  The next a_blocks quantize the rows appended by
+// kattn_decode_append into the cache, one warp per (row, kv head, K or V).
+// The blocks after those write the work list (or, above kFusedListMaxB
+// sequences, one block writes its prefix for list_kernel).
 constexpr int kPrepWarps = 4;
 constexpr int kFusedListMaxB = 2048;              // prepare writes the list itself up to here
 constexpr int kListPerBlock = 1024;               // items per list block of prepare
 
 __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodeParams p,
-                                                                  int q_blocks) {
+                                                                  int q_blocks, int a_blocks) {
   griddep_launch_dependents();                    // the decode grid may start its set-up
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if ((int)blockIdx.x >= q_blocks && (int)blockIdx.x < q_blocks + a_blocks) {
+    // Appended rows: warp (r, kv head, K or V), as kattn_quantize_kv_rows.
+    const int64_t idx = (int64_t)((int)blockIdx.x - q_blocks) * kPrepWarps + warp;
+    if (idx >= (int64_t)p.n_new * p.Hkv * 2) return;
+    const int which = (int)(idx & 1);
+    const int64_t rh = idx >> 1;
+    const int r = (int)(rh / p.Hkv), h = (int)(rh % p.Hkv);
+    const int64_t row = p.dst_rows[r];
+    if (row < 0 || row >= p.cap_rows) return;     // checked here: the index array is on the device
+    const float* src = (which ? p.v_new : p.k_new) + (int64_t)r * p.new_stride + (int64_t)h * kD;
+    warp_quantize_into_cache(src, which ? p.v_w : p.k_w, which ? p.vs_w : p.ks_w,
+                             (int64_t)h * p.cap_rows + row);
+    return;
+  }
   if ((int)blockIdx.x < q_blocks) {
     const int64_t idx = (int64_t)blockIdx.x * kPrepWarps + warp;
     if (idx >= (int64_t)p.B * p.Hkv * p.rpad) return;
@@ -395,7 +412,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodePa
   }
   if (tid == kThreads - 1) {                      // its run ends at B
     pre[p.B] = base;
-    if (!fused || blockIdx.x == (unsigned)q_blocks) *p.item_count = (uint32_t)base;
+    if (!fused || blockIdx.x == (unsigned)(q_blocks + a_blocks)) *p.item_count = (uint32_t)base;
   }
   if (!fused) return;
   // List block k writes items j = k * kThreads + tid, stepping by all list
@@ -403,7 +420,8 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodePa
   // the shared prefix.
   __syncthreads();
   const int total = s_pre[p.B];
-  for (int j = ((int)blockIdx.x - q_blocks) * kThreads + tid; j < total; j += p.list_blocks * kThreads) {
+  for (int j = ((int)blockIdx.x - q_blocks - a_blocks) * kThreads + tid; j < total;
+       j += p.list_blocks * kThreads) {
     int lo = 0, hi = p.B;                         // s_pre[lo] <= j < s_pre[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -1261,8 +1279,9 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
       p.B <= kFusedListMaxB
           ? (int)std::min<int64_t>((max_items + kListPerBlock - 1) / kListPerBlock, 256)
           : 0;
-  prepare_kernel<<<q_blocks + (pp.list_blocks > 0 ? pp.list_blocks : 1), kPrepWarps * 32, 0, stream>>>(
-      pp, q_blocks);
+  const int a_blocks = (int)(((int64_t)p.n_new * p.Hkv * 2 + kPrepWarps - 1) / kPrepWarps);
+  prepare_kernel<<<q_blocks + a_blocks + (pp.list_blocks > 0 ? pp.list_blocks : 1), kPrepWarps * 32,
+                   0, stream>>>(pp, q_blocks, a_blocks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (pp.list_blocks == 0) {

@@ -56,6 +56,18 @@ __device__ __forceinline__ uint32_t warp_quantize_row(const float* __restrict__ 
                    quant_one(x.w, s));
 }
 
+// One warp quantizes a 128-float row into cache row `dst` of the 2-D view
+// [Hkv * cap_rows][128] (int8 bytes and the float scale).
+__device__ __forceinline__ void warp_quantize_into_cache(const float* __restrict__ x_row,
+                                                         int8_t* __restrict__ out_q,
+                                                         float* __restrict__ out_scale,
+                                                         int64_t dst) {
+  float scale;
+  const uint32_t w = warp_quantize_row(x_row, &scale);
+  reinterpret_cast<uint32_t*>(out_q + dst * KATTN_HEAD_DIM)[threadIdx.x & 31] = w;
+  if ((threadIdx.x & 31) == 0) out_scale[dst] = scale;
+}
+
 // Rounding of P before it multiplies V (susun-blog page, section "注意力权重").
 __device__ __forceinline__ float e4m3_round(float x) {
   __nv_fp8_storage_t s = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);

@@ -66,6 +66,16 @@ DecodeParams make_params(const float* q, const int8_t* k, const float* k_scale,
   return p;
 }
 
+void set_workspace(DecodeParams& p, const WorkspaceLayout& w, void* workspace) {
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.err_word = reinterpret_cast<uint32_t*>(ws);
+  p.item_count = reinterpret_cast<uint32_t*>(ws + 4);
+  p.prefix = reinterpret_cast<int*>(ws + w.prefix_off);
+  p.items = reinterpret_cast<int4*>(ws + w.items_off);
+  p.qpack = ws + w.q_off;
+  p.partials = reinterpret_cast<float*>(ws + w.partials_off);
+}
+
 }  // namespace
 
 extern "C" {
@@ -162,15 +172,54 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale, const in
     if ((int64_t)B * w.nsplit_max * Hkv > (int64_t)INT32_MAX / 4) return KATTN_ERR_UNSUPPORTED;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
       return KATTN_ERR_WORKSPACE;
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    p.err_word = reinterpret_cast<uint32_t*>(ws);
-    p.item_count = reinterpret_cast<uint32_t*>(ws + 4);
-    p.prefix = reinterpret_cast<int*>(ws + w.prefix_off);
-    p.items = reinterpret_cast<int4*>(ws + w.items_off);
-    p.qpack = ws + w.q_off;
-    p.partials = reinterpret_cast<float*>(ws + w.partials_off);
+    set_workspace(p, w, workspace);
     e = launch_decode_fast(p, as_stream(stream));
   }
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+}
+
+int kattn_decode_append(const float* q, const float* k_new, const float* v_new,
+                        const int64_t* dst_rows, int n_new, int64_t row_stride_elems, int8_t* k,
+                        float* k_scale, int8_t* v, float* v_scale, const int64_t* row_start,
+                        const int32_t* ctx_len, int B, int M, int Hq, int Hkv, int d,
+                        int cap_rows, int max_ctx, float sm_scale, int p_mode, float* out,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_common(q, k, k_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
+  if (st != KATTN_OK) return st;
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X448) return KATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
+  if (n_new < 0 || row_stride_elems < (int64_t)Hkv * d) return KATTN_ERR_INVALID_ARG;
+  if (n_new > 0 && (!k_new || !v_new || !dst_rows)) return KATTN_ERR_INVALID_ARG;
+  if (n_new > 0 && (!aligned(k_new, 16) || !aligned(v_new, 16) || row_stride_elems % 4 != 0 ||
+                    !aligned(dst_rows, 8)))
+    return KATTN_ERR_MISALIGNED;
+  if (B == 0) {                                   // nothing to decode: the append alone
+    if (n_new == 0) return KATTN_OK;
+    int e = kattn_quantize_kv_rows(k_new, n_new, Hkv, d, row_stride_elems, dst_rows, k, k_scale,
+                                   cap_rows, stream);
+    if (e != KATTN_OK) return e;
+    return kattn_quantize_kv_rows(v_new, n_new, Hkv, d, row_stride_elems, dst_rows, v, v_scale,
+                                  cap_rows, stream);
+  }
+  if (!v || !v_scale || !out) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(v, 16) || !aligned(v_scale, 4) || !aligned(out, 16)) return KATTN_ERR_MISALIGNED;
+  DecodeParams p = make_params(q, k, k_scale, v, v_scale, row_start, ctx_len, B, M, Hq, Hkv,
+                               cap_rows, max_ctx, sm_scale, p_mode, out);
+  const WorkspaceLayout w = workspace_layout(B, M, Hq, max_ctx);
+  if ((int64_t)B * w.nsplit_max * Hkv > (int64_t)INT32_MAX / 4) return KATTN_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
+    return KATTN_ERR_WORKSPACE;
+  set_workspace(p, w, workspace);
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.dst_rows = dst_rows;
+  p.n_new = n_new;
+  p.new_stride = row_stride_elems;
+  p.k_w = k;
+  p.ks_w = k_scale;
+  p.v_w = v;
+  p.vs_w = v_scale;
+  cudaError_t e = launch_decode_fast(p, as_stream(stream));
   return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
 }
 

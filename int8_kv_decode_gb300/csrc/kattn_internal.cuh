@@ -87,6 +87,17 @@ struct DecodeParams {
   int B, M, Hq, Hkv, g, R;
   int rpad;             // row_tile(R)
   int list_blocks;      // > 0: prepare_kernel writes the work items in this many blocks
+  // Rows appended before the decode (kattn_decode_append), n_new = 0 if none:
+  // row r of k_new / v_new goes to cache row dst_rows[r] of every kv head.
+  const float* k_new;
+  const float* v_new;
+  const int64_t* dst_rows;
+  int64_t new_stride;   // floats between rows of k_new / v_new
+  int n_new;
+  int8_t* k_w;          // the caches, writable (the same arrays as k, v)
+  float* ks_w;
+  int8_t* v_w;
+  float* vs_w;
   int cap_rows, max_ctx, nsplit_max;
   float sm_scale;       // already resolved (never 0)
   int p_mode;

@@ -19,11 +19,8 @@ quantize_kv_kernel(const float* __restrict__ x, int n_rows, int n_kv, int64_t ro
   // (checked here because the index array lives on the device).
   const int64_t row = dst_rows ? dst_rows[r] : dst_row0 + r;
   if (row < 0 || row >= cap_rows) return;
-  float scale;
-  const uint32_t w = warp_quantize_row(x + (int64_t)r * row_stride + (int64_t)h * kD, &scale);
-  const int64_t dst = (int64_t)h * cap_rows + row;
-  reinterpret_cast<uint32_t*>(out_q + dst * kD)[threadIdx.x & 31] = w;
-  if ((threadIdx.x & 31) == 0) out_scale[dst] = scale;
+  warp_quantize_into_cache(x + (int64_t)r * row_stride + (int64_t)h * kD, out_q, out_scale,
+                           (int64_t)h * cap_rows + row);
 }
 
 }  // namespace

@@ -358,3 +358,44 @@ def test_full_size_serving_sampled():
             got.append(out[b, j, h])
             ref.append(o[0, j, h])
     assert_f32_tolerance(np.array(got), np.array(ref))
+
+
+@pytest.mark.parametrize("name,p_mode", [("spec_verify", 0), ("spec_verify", 2), ("qwen_layer", 0)])
+def test_decode_append_equals_separate_calls(name, p_mode):
+    # kattn_decode_append: the M draft rows of every sequence quantized into
+    # the cache inside the decode launch -- the same cache bytes and outputs
+    # as kattn_quantize_kv_rows twice followed by kattn_decode.
+    import torch
+    import int8_kv_decode_gb300 as K
+    wl = WORKLOADS[name]
+    x = make_workload(wl, rep=5)
+    dev = "cuda"
+    k_rows = torch.from_numpy(x.k_rows).to(dev)
+    v_rows = torch.from_numpy(x.v_rows).to(dev)
+    # the draft rows of sequence b: row_start + ctx - 1 + j (j < M)
+    dst = torch.tensor([int(x.row_start[b]) + int(x.ctx[b]) - 1 + j
+                        for b in range(wl.B) for j in range(wl.M)], dtype=torch.int64, device=dev)
+    caches = []
+    for _ in range(2):
+        k8 = torch.zeros((wl.Hkv, x.cap_rows, wl.d), dtype=torch.int8, device=dev)
+        v8 = torch.zeros_like(k8)
+        ks = torch.zeros((wl.Hkv, x.cap_rows), dtype=torch.float32, device=dev)
+        vs = torch.zeros_like(ks)
+        K.quantize_kv(k_rows, k8, ks)                 # the prefill, then stale draft rows
+        K.quantize_kv(v_rows, v8, vs)
+        caches.append((k8, ks, v8, vs))
+    knew = torch.randn((dst.numel(), wl.Hkv, wl.d), device=dev) * 2
+    vnew = torch.randn_like(knew)
+    q = torch.from_numpy(x.q).to(dev)
+    rs = torch.from_numpy(x.row_start).to(dev)
+    ctx = torch.from_numpy(x.ctx).to(dev)
+    k8, ks, v8, vs = caches[0]
+    K.quantize_kv_rows(knew, dst, k8, ks)
+    K.quantize_kv_rows(vnew, dst, v8, vs)
+    ref = K.decode(q, k8, ks, v8, vs, rs, ctx, x.max_ctx, p_mode=p_mode).cpu().numpy()
+    k8b, ksb, v8b, vsb = caches[1]
+    got = K.decode_append(q, knew, vnew, dst, k8b, ksb, v8b, vsb, rs, ctx, x.max_ctx,
+                          p_mode=p_mode).cpu().numpy()
+    assert np.array_equal(bits(got), bits(ref))
+    for a, b in zip(caches[0], caches[1]):
+        assert torch.equal(a, b)
