@@ -62,7 +62,8 @@ enum kattn_p_mode {
   KATTN_P_F32 = 0,      /* keep float32 */
   KATTN_P_BF16 = 1,     /* round to bfloat16, nearest-even */
   KATTN_P_E4M3 = 2,     /* round to fp8 e4m3 (OCP), nearest-even, saturating */
-  KATTN_P_E4M3_X448 = 3 /* e4m3(p * 448) / 448 */
+  KATTN_P_E4M3_X448 = 3, /* e4m3(p * 448) / 448 */
+  KATTN_P_E4M3_X256 = 4  /* e4m3(p * 256) / 256 (both scalings exact in float32) */
 };
 
 #define KATTN_HEAD_DIM 128 /* the only supported head_dim */

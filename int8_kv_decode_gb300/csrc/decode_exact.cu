@@ -43,6 +43,7 @@ __device__ __forceinline__ float round_p_exact(float p, int mode) {
     case KATTN_P_BF16: return bf16_round(p);
     case KATTN_P_E4M3: return e4m3_round(p);
     case KATTN_P_E4M3_X448: return __fdiv_rn(e4m3_round(__fmul_rn(p, 448.0f)), 448.0f);
+    case KATTN_P_E4M3_X256: return __fmul_rn(e4m3_round(__fmul_rn(p, 256.0f)), 1.0f / 256.0f);
     default: return p;
   }
 }

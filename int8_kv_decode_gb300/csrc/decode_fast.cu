@@ -232,6 +232,8 @@ __device__ __forceinline__ float round_p_t(float p) {
     return bf16_round(p);
   } else if constexpr (PM == KATTN_P_E4M3) {
     return e4m3_round(p);
+  } else if constexpr (PM == KATTN_P_E4M3_X256) {
+    return __fmul_rn(e4m3_round(__fmul_rn(p, 256.0f)), 1.0f / 256.0f);   // both exact
   } else if constexpr (PM == KATTN_P_E4M3_X448) {
     return __fmul_rn(e4m3_round(__fmul_rn(p, 448.0f)), 1.0f / 448.0f);
   } else {
@@ -1256,6 +1258,7 @@ cudaError_t launch_rows(const DecodeParams& p, const TmaMaps& maps, cudaStream_t
     case KATTN_P_BF16: return launch_variant<NR, NG, KATTN_P_BF16>(p, maps, stream);
     case KATTN_P_E4M3: return launch_variant<NR, NG, KATTN_P_E4M3>(p, maps, stream);
     case KATTN_P_E4M3_X448: return launch_variant<NR, NG, KATTN_P_E4M3_X448>(p, maps, stream);
+    case KATTN_P_E4M3_X256: return launch_variant<NR, NG, KATTN_P_E4M3_X256>(p, maps, stream);
     default: return launch_variant<NR, NG, KATTN_P_F32>(p, maps, stream);
   }
 }

@@ -154,7 +154,7 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale, const in
                  size_t workspace_bytes, void* stream) {
   int st = check_common(q, k, k_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
   if (st != KATTN_OK) return st;
-  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X448) return KATTN_ERR_INVALID_ARG;
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
   if (exact_mode != 0 && exact_mode != 1) return KATTN_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
   if (B == 0) return KATTN_OK;
@@ -186,7 +186,7 @@ int kattn_decode_append(const float* q, const float* k_new, const float* v_new,
                         void* workspace, size_t workspace_bytes, void* stream) {
   int st = check_common(q, k, k_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
   if (st != KATTN_OK) return st;
-  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X448) return KATTN_ERR_INVALID_ARG;
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
   if (n_new < 0 || row_stride_elems < (int64_t)Hkv * d) return KATTN_ERR_INVALID_ARG;
   if (n_new > 0 && (!k_new || !v_new || !dst_rows)) return KATTN_ERR_INVALID_ARG;

@@ -4,7 +4,9 @@ Source: "在 agent 时代如何快速验证 kernel 对精度的影响", section
 "注意力权重：直接转 fp8 随上下文变差，先放大就和 bf16 差不多".  The naive
 kernel there rounds only the P that multiplies V, in one of four ways:
 keep f32, round to bf16, round to fp8 e4m3, or multiply by 448 (the e4m3
-maximum), round to e4m3 and divide the 448 back out.
+maximum), round to e4m3 and divide the 448 back out.  The same section names
+256 as the factor other fp8 attention kernels scale by before the cast; that
+variant is mode 4.
 
 Both formats are written from their definitions, not by bit tricks:
 a value v >= 0 is rounded on the grid of its binade,
@@ -27,7 +29,7 @@ from __future__ import annotations
 import numpy as np
 
 E4M3_MAX = 448.0
-P_MODES = {0: "f32", 1: "bf16", 2: "e4m3", 3: "e4m3x448"}
+P_MODES = {0: "f32", 1: "bf16", 2: "e4m3", 3: "e4m3x448", 4: "e4m3x256"}
 
 
 def _round_grid(v, mbits: int, emin: int):
@@ -57,7 +59,8 @@ def round_p(p, mode: int):
     mode 0: identity; 1: bf16(p); 2: e4m3(p);
     3: e4m3(f32(p * 448)) / 448 -- the product is rounded to float32 first
        (the kernel multiplies in float32), the final division is exact
-       float64 arithmetic on the e4m3 value.
+       float64 arithmetic on the e4m3 value;
+    4: e4m3(p * 256) / 256 -- both scalings by a power of two are exact.
     Returns float64.
     """
     p = np.asarray(p, dtype=np.float32)
@@ -70,6 +73,8 @@ def round_p(p, mode: int):
     if mode == 3:
         scaled = np.multiply(p, np.float32(E4M3_MAX), dtype=np.float32)
         return e4m3(scaled) / E4M3_MAX
+    if mode == 4:
+        return e4m3(np.float64(p) * 256.0) / 256.0
     raise ValueError(f"unknown p_mode {mode}")
 
 

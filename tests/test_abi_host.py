@@ -96,7 +96,7 @@ def test_decode_validation(lib):
     assert _decode(lib, q=0x1008) == MISAL
     assert _decode(lib, k=0x1004) == MISAL
     assert _decode(lib, rs=0x1004) == MISAL
-    assert _decode(lib, p_mode=4) == INVALID
+    assert _decode(lib, p_mode=5) == INVALID
     assert _decode(lib, exact=2) == INVALID
     assert _decode(lib, sm=float("nan")) == INVALID
     assert _decode(lib, max_ctx=0) == INVALID

@@ -77,6 +77,7 @@ def test_qk_scores_bit_exact(name):
 # -------------------------------------------------------------- exact mode --
 
 @pytest.mark.parametrize("name,p_mode", [("tiny", 0), ("tiny", 1), ("tiny", 2), ("tiny", 3),
+                                         ("tiny", 4),
                                          ("qwen_layer", 0), ("qwen_layer", 3)])
 def test_exact_mode_bit_exact(name, p_mode):
     c = upload(WORKLOADS[name])
@@ -111,7 +112,7 @@ def test_fast_f32_spec_verify_sampled():
     assert_f32_tolerance(got, ref, row_mask(got.shape, rows))
 
 
-@pytest.mark.parametrize("p_mode", [1, 2, 3])
+@pytest.mark.parametrize("p_mode", [1, 2, 3, 4])
 @pytest.mark.parametrize("name", ["tiny", "qwen_layer"])
 def test_fast_rounded_p_modes(name, p_mode):
     import int8_kv_decode_gb300 as K

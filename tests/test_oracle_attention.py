@@ -115,7 +115,7 @@ def test_reference_against_brute_force():
                 np.testing.assert_allclose(out[b, j, h], ref, rtol=1e-12, atol=1e-14)
 
 
-@pytest.mark.parametrize("p_mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("p_mode", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("mode", ["reference", "exact"])
 def test_single_key_returns_dequantized_row(p_mode, mode):
     rng = np.random.default_rng(14)

@@ -100,3 +100,40 @@ def test_round_p_modes():
     assert R.round_p(x, 3) == R.e4m3(np.float32(x * np.float32(448))) / 448
     # exact-mode variant divides in float32
     assert R.round_p_f32(x, 3) == np.float32(np.float32(R.e4m3(x * np.float32(448))) / np.float32(448))
+
+
+# -- mode 4: e4m3(p * 256) / 256 ("注意力权重" section: the factor other fp8
+#    attention kernels scale by) -------------------------------------------------
+
+def test_x256_matches_plain_e4m3_where_scaling_commutes():
+    # For p >= 2^-6 both p and 256 p lie in e4m3's normal range below 448,
+    # where scaling by a power of two commutes with rounding.
+    rng = np.random.default_rng(4)
+    p = np.concatenate([rng.uniform(2.0 ** -6, 1.0, 20000), [2.0 ** -6, 0.5, 1.0]]).astype(np.float32)
+    assert np.array_equal(R.round_p(p, 4), R.round_p(p, 2))
+
+
+def test_x256_threshold_and_ties():
+    # smallest nonzero result 2^-9 / 256 = 2^-17; half of it is a tie to 0
+    tiny = np.float32(2.0 ** -17)
+    assert R.round_p(np.array([tiny]), 4)[0] == 2.0 ** -17
+    assert R.round_p(np.array([np.float32(2.0 ** -18)]), 4)[0] == 0.0
+    assert R.round_p(np.array([np.float32(3 * 2.0 ** -19)]), 4)[0] == 2.0 ** -17
+    # p = 1 and the largest values stay exact (256 < 448: no saturation)
+    assert R.round_p(np.array([np.float32(1.0)]), 4)[0] == 1.0
+
+
+def test_x256_brute_force_against_the_e4m3_value_set():
+    # every e4m3 value (positive, finite) / 256 is a fixed point, and a
+    # value between two neighbours goes to the nearer one
+    # E4M3 from its definition: subnormals m * 2^-9 (m = 1..7), normals
+    # (8 + m) * 2^(e - 3) for e = -6..8, m = 0..7, up to 448
+    vals = {m * 2.0 ** -9 for m in range(1, 8)}
+    vals |= {(8 + m) * 2.0 ** (e - 3) for e in range(-6, 9) for m in range(8)}
+    grid = np.array(sorted(v for v in vals if v <= 448.0)) / 256.0
+    assert len(grid) == 126
+    assert np.array_equal(R.round_p(grid.astype(np.float32), 4), grid)
+    mids = (grid[1:-1] + grid[2:]) / 2 * (1 + 1e-6)           # just above a midpoint
+    out = R.round_p(mids.astype(np.float32), 4)
+    assert np.array_equal(out, grid[2:])
+    assert np.array_equal(R.round_p_f32(grid.astype(np.float32), 4).astype(np.float64), grid)
