@@ -240,6 +240,16 @@ int kattn_qk_scores_debug(const float* q, const int8_t* k, const float* k_scale,
  * out68 is NULL. */
 int kattn_expf_constants(double* out68);
 
+/* Row hashes for parity dumps ("Kestrel_VLLM - 18" §3.4: hash buffers on
+ * both sides with the same FNV-1a 64, compare the lists, and the first
+ * difference localises the divergence).  hashes[r] = FNV-1a 64 (offset basis
+ * 14695981039346656037, prime 1099511628211) of the row_bytes bytes at
+ * data + r * row_stride_bytes, in address order.  data, hashes: device
+ * pointers (hashes 8-byte aligned, n_rows entries).  The library has no
+ * counterpart in the pages' decode path; it is test tooling. */
+int kattn_hash_rows(const void* data, int64_t n_rows, int64_t row_bytes, int64_t row_stride_bytes,
+                    uint64_t* hashes, void* stream);
+
 /* Read (and clear) the device error word of a decode workspace.  Copies 4
  * bytes to the host and waits for `stream`.  *device_err receives the
  * KATTN_DEVERR_* bits set by calls since the last read. */

@@ -13,6 +13,7 @@ from .api import (  # noqa: F401
     expf_constants,
     get_device_status,
     get_tiling,
+    hash_rows,
     qk_scores_debug,
     quantize_kv,
     quantize_kv_rows,

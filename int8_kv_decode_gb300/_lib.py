@@ -38,6 +38,7 @@ SIGNATURES = {
                                       c_int, c_int, c_int, c_int, c_int, c_int, c_void_p,
                                       c_void_p, c_void_p, c_void_p]),
     "kattn_expf_constants": (c_int, [ctypes.POINTER(ctypes.c_double)]),
+    "kattn_hash_rows": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     "kattn_get_device_status": (c_int, [c_void_p, c_size_t, ctypes.POINTER(c_int), c_void_p]),
 }
 

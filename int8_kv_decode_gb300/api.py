@@ -181,6 +181,24 @@ def decode_append(q, k_new, v_new, dst_rows, k, k_scale, v, v_scale, row_start, 
     return out
 
 
+def hash_rows(x: torch.Tensor) -> torch.Tensor:
+    """FNV-1a 64 of every row of x (a CUDA tensor whose last dimension is
+    contiguous; rows = all leading indices).  Returns int64 [rows] holding
+    the uint64 hash bits (kattn_hash_rows)."""
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    x2 = x.reshape(-1, x.shape[-1]) if x.dim() > 1 else x.reshape(1, -1)
+    if x2.stride(-1) != 1:
+        raise ValueError("the last dimension of x must be contiguous")
+    out = torch.empty(x2.shape[0], dtype=torch.int64, device=x.device)
+    row_bytes = x2.shape[1] * x2.element_size()
+    stride = x2.stride(0) * x2.element_size()
+    lib = _lib.load()
+    _lib.check("kattn_hash_rows", lib.kattn_hash_rows(
+        _ptr(x2), x2.shape[0], row_bytes, stride, _ptr(out), _stream(x.device)))
+    return out
+
+
 def qk_scores_debug(q, k, k_scale, row_start, ctx_len, max_ctx: int, *, scores=None,
                     want_q=False):
     """Integer QK scores [B][M][Hq][max_ctx + M - 1] (int32); entries t >= L_j

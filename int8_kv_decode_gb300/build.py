@@ -34,6 +34,7 @@ SOURCES = {
     "decode_noalloc.cu": [],
     "decode_exact.cu": ["--fmad=false"],
     "expf_constants.cu": ["--fmad=false"],
+    "hash_rows.cu": [],
 }
 
 

@@ -239,6 +239,17 @@ int kattn_qk_scores_debug(const float* q, const int8_t* k, const float* k_scale,
   return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
 }
 
+int kattn_hash_rows(const void* data, int64_t n_rows, int64_t row_bytes, int64_t row_stride_bytes,
+                    uint64_t* hashes, void* stream) {
+  if (n_rows < 0 || row_bytes < 0 || row_stride_bytes < row_bytes) return KATTN_ERR_INVALID_ARG;
+  if (n_rows == 0) return KATTN_OK;
+  if (!data || !hashes) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(hashes, 8)) return KATTN_ERR_MISALIGNED;
+  const cudaError_t e = launch_hash_rows(data, n_rows, row_bytes, row_stride_bytes, hashes,
+                                         as_stream(stream));
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+}
+
 int kattn_get_device_status(void* workspace, size_t workspace_bytes, int* device_err,
                             void* stream) {
   if (!workspace || !device_err || workspace_bytes < 256) return KATTN_ERR_INVALID_ARG;

@@ -119,6 +119,8 @@ cudaError_t launch_quantize_kv(const float* x, int n_rows, int n_kv, int64_t row
 cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_exact(const DecodeParams& p, const ExpfConsts& c,
                                 cudaStream_t stream);
+cudaError_t launch_hash_rows(const void* data, int64_t n_rows, int64_t row_bytes, int64_t stride,
+                             uint64_t* out, cudaStream_t stream);
 cudaError_t launch_qk_debug(const DecodeParams& p, int32_t* scores, int8_t* q_i8,
                             float* q_scale, cudaStream_t stream);
 

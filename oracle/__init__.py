@@ -19,15 +19,17 @@ Sources (page title, then section):
 
 Modules:
   quant      -- per-row absmax/127 int8 quantization (K/V rows and queries)
-  rounding   -- bf16 and fp8-e4m3 round-to-nearest-even, the four round_p
+  rounding   -- bf16 and fp8-e4m3 round-to-nearest-even, the round_p modes
   expf_tang  -- the table-driven exp (64-entry 2^(j/64) table, 3-term poly)
   attention  -- QK scores, reference decode (float64, with the rounding
                 points mirrored for rounded-P modes) and the exact-mode
                 float32 emulation
+  hashdump   -- FNV-1a 64 row hashes and the first differing row (§3.4's
+                parity-dump method)
 
 Parity unpinned: the absolute accuracy of the rounded-P modes against the
 infinitely precise softmax is not pinned by anything on the pages; only the
 same-rounding comparison is.
 """
 
-from . import quant, rounding, expf_tang, attention  # noqa: F401
+from . import quant, rounding, expf_tang, attention, hashdump  # noqa: F401

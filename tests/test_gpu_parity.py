@@ -400,3 +400,27 @@ def test_decode_append_equals_separate_calls(name, p_mode):
     assert np.array_equal(bits(got), bits(ref))
     for a, b in zip(caches[0], caches[1]):
         assert torch.equal(a, b)
+
+
+def test_row_hashes_match_the_oracle_and_find_a_planted_divergence():
+    # kattn_hash_rows (FNV-1a 64 per row, "Kestrel_VLLM - 18" §3.4) against the
+    # oracle's hashes of the same bytes: the quantized K cache, the exact-mode
+    # output, and strided / misaligned row views.
+    import torch
+    import int8_kv_decode_gb300 as K
+    from oracle import hashdump as H
+    c = upload(WORKLOADS["qwen_layer"])
+    k_bytes = c.k8.reshape(-1, 128)
+    assert np.array_equal(K.hash_rows(k_bytes).cpu().numpy().view(np.uint64),
+                          H.hash_rows(c.ok8.reshape(-1, 128)))
+    ex = run(c, exact_mode=True)
+    ref = oracle_decode(c, mode="exact").astype(np.float32)
+    gh = K.hash_rows(ex.reshape(-1, 128)).cpu().numpy().view(np.uint64)
+    assert H.first_divergence(gh, H.hash_rows(ref.reshape(-1, 128))) is None
+    planted = ref.reshape(-1, 128).copy()
+    planted[17, 3] = np.nextafter(planted[17, 3], np.float32(np.inf))
+    assert H.first_divergence(gh, H.hash_rows(planted)) == 17
+    # a strided view whose rows start 4 bytes past 16-byte boundaries
+    view = ex.reshape(-1, 128)[:, 1:101]
+    assert np.array_equal(K.hash_rows(view).cpu().numpy().view(np.uint64),
+                          H.hash_rows(ex.reshape(-1, 128)[:, 1:101].cpu().numpy()))
