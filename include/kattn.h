@@ -74,6 +74,8 @@ enum kattn_p_mode {
 #define KATTN_DEVERR_BAD_SEQUENCE 0x1u /* row_start / ctx_len out of range */
 #define KATTN_DEVERR_TIMEOUT 0x2u      /* a bounded wait for a K/V block ran out;
                                           the affected outputs are not written */
+#define KATTN_DEVERR_BAD_PAGE 0x4u     /* kattn_decode_paged: a block-table entry
+                                          outside [0, cap_rows / page_rows) */
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* kattn_status_string(int status);
@@ -170,6 +172,31 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale,
                  int cap_rows, int max_ctx, float sm_scale, int p_mode,
                  int exact_mode, float* out, void* workspace,
                  size_t workspace_bytes, void* stream);
+
+/* kattn_decode over a paged cache: the same computation, with key t of
+ * sequence b at row
+ *   block_table[b * max_pages + t / page_rows] * page_rows + t % page_rows
+ * of head kh's plane of k, v, k_scale, v_scale (shapes as kattn_decode;
+ * cap_rows = pages * page_rows).  Keys sit at the same positions of the
+ * fixed tiling as in the contiguous layout, so out equals, byte for byte,
+ * kattn_decode on a cache holding the same rows contiguously.
+ * block_table: int32 [B][max_pages] on the device, 4-byte aligned.
+ * page_rows:   32 * 2^k (a 32-key TMA block never crosses a page), dividing
+ *              cap_rows; other powers of two or smaller pages ->
+ *              KATTN_ERR_UNSUPPORTED.
+ * Checked on the device: ctx_len[b] in [1, max_ctx] and
+ *   ceil((ctx_len[b] + M - 1) / page_rows) <= max_pages, else NaN outputs
+ *   and KATTN_DEVERR_BAD_SEQUENCE as in kattn_decode; a table entry read
+ *   outside [0, cap_rows / page_rows) sets KATTN_DEVERR_BAD_PAGE (fast mode)
+ *   and reads page 0 instead: the outputs of that sequence are then
+ *   unspecified, and no access leaves the arrays.
+ * Other arguments, modes, workspace and errors as kattn_decode. */
+int kattn_decode_paged(const float* q, const int8_t* k, const float* k_scale, const int8_t* v,
+                       const float* v_scale, const int32_t* block_table, int max_pages,
+                       int page_rows, const int32_t* ctx_len, int B, int M, int Hq, int Hkv,
+                       int d, int cap_rows, int max_ctx, float sm_scale, int p_mode,
+                       int exact_mode, float* out, void* workspace, size_t workspace_bytes,
+                       void* stream);
 
 /* One decode step with its KV append: kattn_quantize_kv_rows of k_new into
  * (k, k_scale) and of v_new into (v, v_scale), then kattn_decode in fast mode

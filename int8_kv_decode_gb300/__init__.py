@@ -9,6 +9,7 @@ from .api import (  # noqa: F401
     alloc_workspace,
     decode,
     decode_append,
+    decode_paged,
     decode_workspace_size,
     expf_constants,
     get_device_status,

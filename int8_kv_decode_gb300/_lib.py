@@ -27,6 +27,10 @@ SIGNATURES = {
     "kattn_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                              c_float, c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "kattn_decode_paged": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                   c_int, c_int, c_float, c_int, c_int, c_void_p, c_void_p,
+                                   c_size_t, c_void_p]),
     "kattn_decode_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int64,
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float,

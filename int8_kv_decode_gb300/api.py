@@ -141,6 +141,49 @@ def decode(q, k, k_scale, v, v_scale, row_start, ctx_len, max_ctx: int, *,
     return out
 
 
+def decode_paged(q, k, k_scale, v, v_scale, block_table, page_rows: int, ctx_len, max_ctx: int,
+                 *, out=None, p_mode=0, exact_mode=False, sm_scale: float = 0.0, workspace=None):
+    """Decode attention over a paged cache; returns out [B][M][Hq][d] float32.
+
+    Key t of sequence b is row block_table[b][t // page_rows] * page_rows +
+    t % page_rows of every kv-head plane of k, v [Hkv][cap][d] (int8) and
+    k_scale, v_scale [Hkv][cap] (f32).  block_table: int32 [B][max_pages];
+    page_rows: 32 * 2^k, dividing cap.  Otherwise as decode().
+    """
+    _need(q, torch.float32, "q", 4)
+    _need(k, torch.int8, "k", 3)
+    _need(v, torch.int8, "v", 3)
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(v_scale, torch.float32, "v_scale", 2)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(ctx_len, torch.int32, "ctx_len", 1)
+    B, M, Hq, d = q.shape
+    Hkv, cap, _ = k.shape
+    if tuple(v.shape) != tuple(k.shape) or tuple(k_scale.shape) != (Hkv, cap) \
+            or tuple(v_scale.shape) != (Hkv, cap):
+        raise ValueError("k/v/scales shapes disagree")
+    if block_table.shape[0] != B or ctx_len.numel() != B:
+        raise ValueError("block_table / ctx_len must have B rows")
+    mode = P_MODES.get(p_mode, p_mode) if isinstance(p_mode, str) else int(p_mode)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, torch.float32, "out", 4)
+    ws_bytes = 0
+    if not exact_mode:
+        if workspace is None:
+            workspace = alloc_workspace(B, M, Hq, max_ctx, q.device)
+        _need(workspace, torch.uint8, "workspace", 1)
+        ws_bytes = workspace.numel()
+    lib = _lib.load()
+    _lib.check("kattn_decode_paged", lib.kattn_decode_paged(
+        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(v), _ptr(v_scale), _ptr(block_table),
+        int(block_table.shape[1]), int(page_rows), _ptr(ctx_len), B, M, Hq, Hkv, d, cap,
+        int(max_ctx), float(sm_scale), mode, 1 if exact_mode else 0, _ptr(out),
+        _ptr(workspace) if not exact_mode else 0, ws_bytes, _stream(q.device)))
+    return out
+
+
 def decode_append(q, k_new, v_new, dst_rows, k, k_scale, v, v_scale, row_start, ctx_len,
                   max_ctx: int, *, out=None, p_mode=0, sm_scale: float = 0.0, workspace=None):
     """Append rows k_new / v_new [n][Hkv][d] f32 at cache rows dst_rows [n]

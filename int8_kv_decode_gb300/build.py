@@ -31,6 +31,7 @@ SOURCES = {
     "quantize.cu": [],
     "qk_debug.cu": [],
     "decode_fast.cu": [],
+    "decode_fast_paged.cu": [],
     "decode_noalloc.cu": [],
     "decode_exact.cu": ["--fmad=false"],
     "expf_constants.cu": ["--fmad=false"],

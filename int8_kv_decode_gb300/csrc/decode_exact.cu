@@ -55,6 +55,7 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   __shared__ float red[kChunk / 32];
   __shared__ float s_alpha[kChunk], s_p[kChunk], s_pr[kChunk], s_vs[kChunk];
   __shared__ float s_carry;
+  __shared__ int s_row[kChunk];                   // plane rows of the chunk's keys
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -65,13 +66,12 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   const int64_t qrow = ((int64_t)b * p.M + j) * p.Hq + h;
   float* orow = p.out + qrow * kD;
 
-  const int64_t rs = p.row_start[b];
-  const int ctx = p.ctx_len[b];
-  if (!sequence_ok(rs, ctx, p.M, p.cap_rows, p.max_ctx)) {
+  if (!sequence_valid(p, b)) {
     orow[tid] = __int_as_float(0x7fc00000);
     return;
   }
-  const int L = ctx + j;
+  const int L = p.ctx_len[b] + j;
+  const int rs = sequence_row0(p, b);
 
   for (int i = tid; i < (int)(sizeof(ExpfConsts) / sizeof(double)); i += kChunk)
     reinterpret_cast<double*>(&c)[i] = reinterpret_cast<const double*>(&consts)[i];
@@ -87,18 +87,22 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   if (tid == 0) s_carry = -INFINITY;
   __syncthreads();
 
-  const int8_t* kbase = p.k + ((int64_t)kh * p.cap_rows + rs) * kD;
-  const int8_t* vbase = p.v + ((int64_t)kh * p.cap_rows + rs) * kD;
-  const float* ksb = p.k_scale + (int64_t)kh * p.cap_rows + rs;
-  const float* vsb = p.v_scale + (int64_t)kh * p.cap_rows + rs;
+  // Key t is row `row` of head kh's plane: rs + t, or from the block table.
+  const int64_t plane = (int64_t)kh * p.cap_rows;
+  const int8_t* kbase = p.k + plane * kD;
+  const int8_t* vbase = p.v + plane * kD;
+  const float* ksb = p.k_scale + plane;
+  const float* vsb = p.v_scale + plane;
 
   float o = 0.0f, l = 0.0f;
   for (int t0 = 0; t0 < L; t0 += kChunk) {
     const int t = t0 + tid;
     const bool live = t < L;
     float s = -INFINITY;
+    const int row = !live ? 0 : p.block_table == nullptr ? rs + t : paged_row(p, b, t);
+    s_row[tid] = row;
     if (live) {
-      const int4* krow = reinterpret_cast<const int4*>(kbase + (int64_t)t * kD);
+      const int4* krow = reinterpret_cast<const int4*>(kbase + (int64_t)row * kD);
       int acc = 0;
 #pragma unroll
       for (int cc = 0; cc < kD / 16; ++cc) {
@@ -108,7 +112,7 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
         acc = __dp4a((int)kv.z, (int)q8[4 * cc + 2], acc);
         acc = __dp4a((int)kv.w, (int)q8[4 * cc + 3], acc);
       }
-      s = __fmul_rn(__fmul_rn((float)acc, __fmul_rn(qs, ksb[t])), p.sm_scale);
+      s = __fmul_rn(__fmul_rn((float)acc, __fmul_rn(qs, ksb[row])), p.sm_scale);
     }
     // Inclusive prefix max over the chunk, seeded with the running max.
     float pm = s;
@@ -136,14 +140,14 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
       s_alpha[tid] = a;
       s_p[tid] = pp;
       s_pr[tid] = round_p_exact(pp, p.p_mode);
-      s_vs[tid] = vsb[t];
+      s_vs[tid] = vsb[row];
     }
     __syncthreads();
     if (tid == min(kChunk, L - t0) - 1) s_carry = pm;
     const int n = min(kChunk, L - t0);
     for (int u = 0; u < n; ++u) {
       const float a = s_alpha[u];
-      const float vdeq = __fmul_rn((float)vbase[(int64_t)(t0 + u) * kD + tid], s_vs[u]);
+      const float vdeq = __fmul_rn((float)vbase[(int64_t)s_row[u] * kD + tid], s_vs[u]);
       o = __fadd_rn(__fmul_rn(o, a), __fmul_rn(s_pr[u], vdeq));
       l = __fadd_rn(__fmul_rn(l, a), s_p[u]);
     }

@@ -86,6 +86,36 @@ __device__ __forceinline__ bool sequence_ok(int64_t rs, int ctx, int M, int cap_
          rs + (int64_t)ctx + (int64_t)(M - 1) <= (int64_t)cap_rows;
 }
 
+// Whether every key of sequence b lies in the cache, in either layout: the
+// contiguous rows [row_start, row_start + ctx + M - 1), or the first
+// ceil((ctx + M - 1) / page) entries of its block-table row.  (The entries
+// themselves are checked where they are read: paged_row.)
+__device__ __forceinline__ bool sequence_valid(const DecodeParams& p, int b) {
+  const int ctx = p.ctx_len[b];
+  if (p.block_table == nullptr) return sequence_ok(p.row_start[b], ctx, p.M, p.cap_rows, p.max_ctx);
+  if (ctx < 1 || ctx > p.max_ctx) return false;
+  const int64_t keys = (int64_t)ctx + p.M - 1;
+  return ((keys + (1 << p.page_shift) - 1) >> p.page_shift) <= (int64_t)p.max_pages;
+}
+
+// Row of key `key` of sequence b within its kv-head plane (paged layout).  An
+// entry outside the cache sets KATTN_DEVERR_BAD_PAGE and reads page 0, so no
+// access leaves the arrays.
+__device__ __forceinline__ int paged_row(const DecodeParams& p, int b, int key) {
+  int page = __ldg(p.block_table + (int64_t)b * p.max_pages + (key >> p.page_shift));
+  if ((unsigned)page >= (unsigned)p.n_pages) {
+    if (p.err_word) atomicOr(p.err_word, KATTN_DEVERR_BAD_PAGE);
+    page = 0;
+  }
+  return (page << p.page_shift) | (key & ((1 << p.page_shift) - 1));
+}
+
+// Row of key 0 of sequence b within its plane: the contiguous layout's
+// row_start; 0 when paged (rows then come from paged_row).
+__device__ __forceinline__ int sequence_row0(const DecodeParams& p, int b) {
+  return p.block_table == nullptr ? (int)p.row_start[b] : 0;
+}
+
 // ------------------------------------------------------------ cp.async ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -18,10 +18,12 @@ float resolve_sm_scale(float sm_scale, int d) {
   return sm_scale != 0.0f ? sm_scale : (float)(1.0 / std::sqrt((double)d));
 }
 
-// Shared argument checks of kattn_decode and kattn_qk_scores_debug.
-int check_common(const float* q, const int8_t* k, const float* k_scale,
-                 const int64_t* row_start, const int32_t* ctx_len, int B, int M, int Hq,
-                 int Hkv, int d, int cap_rows, int max_ctx) {
+// Shared argument checks of the decode entry points and kattn_qk_scores_debug.
+// seq_rows is row_start (int64, contiguous layout) or block_table (int32,
+// paged layout), aligned to seq_align bytes.
+int check_common(const float* q, const int8_t* k, const float* k_scale, const void* seq_rows,
+                 size_t seq_align, const int32_t* ctx_len, int B, int M, int Hq, int Hkv, int d,
+                 int cap_rows, int max_ctx) {
   if (B < 0 || M < 1 || Hq < 1 || Hkv < 1 || cap_rows < 1 || max_ctx < 1)
     return KATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || B > 65535 || Hkv > 65535) return KATTN_ERR_INVALID_ARG;
@@ -31,8 +33,8 @@ int check_common(const float* q, const int8_t* k, const float* k_scale,
   // the fast path addresses cache rows of all heads with int32 TMA coordinates
   if ((int64_t)Hkv * cap_rows > (int64_t)INT32_MAX - 4096) return KATTN_ERR_UNSUPPORTED;
   if (B == 0) return KATTN_OK;
-  if (!q || !k || !k_scale || !row_start || !ctx_len) return KATTN_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(k_scale, 4) || !aligned(row_start, 8) ||
+  if (!q || !k || !k_scale || !seq_rows || !ctx_len) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(k_scale, 4) || !aligned(seq_rows, seq_align) ||
       !aligned(ctx_len, 4))
     return KATTN_ERR_MISALIGNED;
   return KATTN_OK;
@@ -64,6 +66,34 @@ DecodeParams make_params(const float* q, const int8_t* k, const float* k_scale,
   p.sm_scale = resolve_sm_scale(sm_scale, KATTN_HEAD_DIM);
   p.p_mode = p_mode;
   return p;
+}
+
+void set_workspace(DecodeParams& p, const WorkspaceLayout& w, void* workspace);
+
+// The decode proper, once the layout-specific arguments are in p: the checks
+// kattn_decode and kattn_decode_paged share, then the exact or the fast path.
+int run_decode(DecodeParams& p, int p_mode, int exact_mode, float sm_scale, const int8_t* v,
+               const float* v_scale, float* out, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
+  if (exact_mode != 0 && exact_mode != 1) return KATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
+  if (p.B == 0) return KATTN_OK;
+  if (!v || !v_scale || !out) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(v, 16) || !aligned(v_scale, 4) || !aligned(out, 16)) return KATTN_ERR_MISALIGNED;
+  cudaError_t e;
+  if (exact_mode) {
+    e = launch_decode_exact(p, expf_constants(), as_stream(stream));
+  } else {
+    const WorkspaceLayout w = workspace_layout(p.B, p.M, p.Hq, p.max_ctx);
+    // work items x kv heads are counted in int32 on the device
+    if ((int64_t)p.B * w.nsplit_max * p.Hkv > (int64_t)INT32_MAX / 4) return KATTN_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
+      return KATTN_ERR_WORKSPACE;
+    set_workspace(p, w, workspace);
+    e = launch_decode_fast(p, as_stream(stream));
+  }
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
 }
 
 void set_workspace(DecodeParams& p, const WorkspaceLayout& w, void* workspace) {
@@ -152,30 +182,35 @@ int kattn_decode(const float* q, const int8_t* k, const float* k_scale, const in
                  int B, int M, int Hq, int Hkv, int d, int cap_rows, int max_ctx,
                  float sm_scale, int p_mode, int exact_mode, float* out, void* workspace,
                  size_t workspace_bytes, void* stream) {
-  int st = check_common(q, k, k_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
+  int st = check_common(q, k, k_scale, row_start, 8, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
   if (st != KATTN_OK) return st;
-  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
-  if (exact_mode != 0 && exact_mode != 1) return KATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
-  if (B == 0) return KATTN_OK;
-  if (!v || !v_scale || !out) return KATTN_ERR_INVALID_ARG;
-  if (!aligned(v, 16) || !aligned(v_scale, 4) || !aligned(out, 16)) return KATTN_ERR_MISALIGNED;
-
   DecodeParams p = make_params(q, k, k_scale, v, v_scale, row_start, ctx_len, B, M, Hq, Hkv,
                                cap_rows, max_ctx, sm_scale, p_mode, out);
-  cudaError_t e;
-  if (exact_mode) {
-    e = launch_decode_exact(p, expf_constants(), as_stream(stream));
-  } else {
-    const WorkspaceLayout w = workspace_layout(B, M, Hq, max_ctx);
-    // work items x kv heads are counted in int32 on the device
-    if ((int64_t)B * w.nsplit_max * Hkv > (int64_t)INT32_MAX / 4) return KATTN_ERR_UNSUPPORTED;
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
-      return KATTN_ERR_WORKSPACE;
-    set_workspace(p, w, workspace);
-    e = launch_decode_fast(p, as_stream(stream));
-  }
-  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+  return run_decode(p, p_mode, exact_mode, sm_scale, v, v_scale, out, workspace, workspace_bytes,
+                    stream);
+}
+
+int kattn_decode_paged(const float* q, const int8_t* k, const float* k_scale, const int8_t* v,
+                       const float* v_scale, const int32_t* block_table, int max_pages,
+                       int page_rows, const int32_t* ctx_len, int B, int M, int Hq, int Hkv,
+                       int d, int cap_rows, int max_ctx, float sm_scale, int p_mode,
+                       int exact_mode, float* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  int st = check_common(q, k, k_scale, block_table, 4, ctx_len, B, M, Hq, Hkv, d, cap_rows,
+                        max_ctx);
+  if (st != KATTN_OK) return st;
+  if (max_pages < 1 || page_rows < 1) return KATTN_ERR_INVALID_ARG;
+  // a TMA block of 32 keys must lie inside one page
+  if (page_rows < kBlockBk || (page_rows & (page_rows - 1)) != 0) return KATTN_ERR_UNSUPPORTED;
+  if (cap_rows % page_rows != 0) return KATTN_ERR_INVALID_ARG;
+  DecodeParams p = make_params(q, k, k_scale, v, v_scale, nullptr, ctx_len, B, M, Hq, Hkv,
+                               cap_rows, max_ctx, sm_scale, p_mode, out);
+  p.block_table = block_table;
+  p.max_pages = max_pages;
+  p.page_shift = __builtin_ctz((unsigned)page_rows);
+  p.n_pages = cap_rows / page_rows;
+  return run_decode(p, p_mode, exact_mode, sm_scale, v, v_scale, out, workspace, workspace_bytes,
+                    stream);
 }
 
 int kattn_decode_append(const float* q, const float* k_new, const float* v_new,
@@ -184,7 +219,7 @@ int kattn_decode_append(const float* q, const float* k_new, const float* v_new,
                         const int32_t* ctx_len, int B, int M, int Hq, int Hkv, int d,
                         int cap_rows, int max_ctx, float sm_scale, int p_mode, float* out,
                         void* workspace, size_t workspace_bytes, void* stream) {
-  int st = check_common(q, k, k_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
+  int st = check_common(q, k, k_scale, row_start, 8, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
   if (st != KATTN_OK) return st;
   if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
@@ -227,7 +262,7 @@ int kattn_qk_scores_debug(const float* q, const int8_t* k, const float* k_scale,
                           const int64_t* row_start, const int32_t* ctx_len, int B, int M,
                           int Hq, int Hkv, int d, int cap_rows, int max_ctx, int32_t* scores,
                           int8_t* q_i8, float* q_scale, void* stream) {
-  int st = check_common(q, k, k_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
+  int st = check_common(q, k, k_scale, row_start, 8, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
   if (st != KATTN_OK) return st;
   if (B == 0) return KATTN_OK;
   if (!scores) return KATTN_ERR_INVALID_ARG;

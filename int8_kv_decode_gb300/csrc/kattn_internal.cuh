@@ -75,8 +75,13 @@ struct DecodeParams {
   const float* k_scale;
   const int8_t* v;
   const float* v_scale;
-  const int64_t* row_start;
+  const int64_t* row_start;   // contiguous layout (block_table == nullptr)
   const int32_t* ctx_len;
+  // Paged layout: key t of sequence b is row
+  // (block_table[b * max_pages + (t >> page_shift)] << page_shift) + (t & (page - 1))
+  // of its kv-head plane; n_pages = cap_rows >> page_shift.
+  const int32_t* block_table;
+  int max_pages, page_shift, n_pages;
   float* out;
   uint32_t* err_word;   // workspace header (fast mode), may be null in exact mode
   uint32_t* item_count; // workspace header + 4

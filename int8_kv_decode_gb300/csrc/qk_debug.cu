@@ -14,9 +14,9 @@ qk_debug_kernel(DecodeParams p, int32_t* __restrict__ scores, int8_t* __restrict
   const int j = blockIdx.y / p.Hq;
   const int h = blockIdx.y % p.Hq;
   const int kh = h / p.g;
-  const int64_t rs = p.row_start[b];
+  const int64_t rs = p.row_start[b];            // contiguous layout only
   const int ctx = p.ctx_len[b];
-  if (!sequence_ok(rs, ctx, p.M, p.cap_rows, p.max_ctx)) return;
+  if (!sequence_valid(p, b)) return;
   const int L = ctx + j;
   const int64_t qrow = ((int64_t)b * p.M + j) * p.Hq + h;
   if (threadIdx.x < 32) {

@@ -107,6 +107,34 @@ def test_decode_validation(lib):
     assert _decode(lib, B=0) == 0                          # empty batch: no-op
 
 
+def _decode_paged(lib, **kw):
+    a = dict(q=64, k=64, ks=64, v=64, vs=64, bt=64, max_pages=8, page=32, ctx=64, B=1, M=1,
+             Hq=8, Hkv=2, d=128, cap=256, max_ctx=256, sm=0.0, p_mode=0, exact=0, out=64,
+             ws=0, ws_bytes=0, stream=0)
+    a.update(kw)
+    return lib.kattn_decode_paged(a["q"], a["k"], a["ks"], a["v"], a["vs"], a["bt"],
+                                  a["max_pages"], a["page"], a["ctx"], a["B"], a["M"], a["Hq"],
+                                  a["Hkv"], a["d"], a["cap"], a["max_ctx"], a["sm"],
+                                  a["p_mode"], a["exact"], a["out"], a["ws"], a["ws_bytes"],
+                                  a["stream"])
+
+
+def test_decode_paged_validation(lib):
+    # Checked on the host before any CUDA call: the pointers are never used.
+    INVALID, UNSUP, MISAL, WS = -1, -2, -3, -4
+    assert _decode_paged(lib, bt=0) == INVALID
+    assert _decode_paged(lib, bt=0x1002) == MISAL          # int32 table
+    assert _decode_paged(lib, max_pages=0) == INVALID
+    assert _decode_paged(lib, page=0) == INVALID
+    assert _decode_paged(lib, page=16) == UNSUP            # a 32-key block would cross pages
+    assert _decode_paged(lib, page=96, cap=288) == UNSUP   # not a power of two
+    assert _decode_paged(lib, page=64, cap=224) == INVALID  # pages do not tile the planes
+    assert _decode_paged(lib, d=64) == UNSUP
+    assert _decode_paged(lib, p_mode=5) == INVALID
+    assert _decode_paged(lib, ws=0) == WS
+    assert _decode_paged(lib, B=0) == 0
+
+
 def test_quantize_validation(lib):
     f = lib.kattn_quantize_kv
     assert f(64, 4, 2, 64, 256, 64, 64, 0, 8, 0) == -2       # d != 128

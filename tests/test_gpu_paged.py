@@ -1,0 +1,127 @@
+"""Paged KV (kattn_decode_paged) on the GPU.
+
+A paged cache holds the same rows as a contiguous one, at the same key
+positions of the fixed tiling, so the decode must return the same bytes:
+the fast path against kattn_decode on the contiguous cache (itself held to
+the oracle by test_gpu_parity.py), exact mode against the oracle directly.
+Pages are shuffled over the pool, the unused rows hold random bytes and the
+unused table entries are -1, so a read of anything else shows up.
+"""
+
+import numpy as np
+import pytest
+
+from helpers import custom, oracle_decode, run, upload
+from synth import WORKLOADS, make_workload
+from synth.paging import page_layout, paged_copy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def bits(a):
+    return np.ascontiguousarray(np.asarray(a, np.float32)).view(np.uint32)
+
+
+class Paged:
+    def __init__(self, c, P, seed=0):
+        import torch
+        x = c.x
+        self.layout = page_layout(x.ctx, x.row_start, x.wl.M, P, seed=seed)
+        self.k8, self.ks, self.v8, self.vs = paged_copy(self.layout, c.k8, c.ks, c.v8, c.vs,
+                                                        seed=seed)
+        self.bt = torch.from_numpy(self.layout.block_table).to(c.k8.device)
+        self.P = P
+
+    def decode(self, c, bt=None, ctx=None, **kw):
+        import int8_kv_decode_gb300 as K
+        return K.decode_paged(c.q, self.k8, self.ks, self.v8, self.vs,
+                              self.bt if bt is None else bt, self.P,
+                              c.ctx if ctx is None else ctx, c.x.max_ctx, **kw)
+
+
+@pytest.mark.parametrize("p_mode", [0, 2, 3])
+@pytest.mark.parametrize("name,P", [("tiny", 32), ("qwen_layer", 128), ("spec_verify", 32),
+                                    ("spec_verify", 256)])
+def test_paged_equals_contiguous_bytes(name, P, p_mode):
+    import int8_kv_decode_gb300 as K
+    c = upload(WORKLOADS[name])
+    ref = run(c, p_mode=p_mode).cpu().numpy()
+    pc = Paged(c, P, seed=P + p_mode)
+    wl = c.x.wl
+    ws = K.alloc_workspace(wl.B, wl.M, wl.Hq, c.x.max_ctx)
+    got = pc.decode(c, p_mode=p_mode, workspace=ws).cpu().numpy()
+    assert np.array_equal(bits(got), bits(ref))
+    assert K.get_device_status(ws) == 0          # no -1 entry or spare page was read
+
+
+@pytest.mark.parametrize("name,P,p_mode", [("tiny", 32, 0), ("tiny", 64, 2), ("qwen_layer", 128, 0),
+                                           ("qwen_layer", 32, 3)])
+def test_paged_exact_mode_bit_exact(name, P, p_mode):
+    c = upload(WORKLOADS[name])
+    got = Paged(c, P, seed=7).decode(c, p_mode=p_mode, exact_mode=True).cpu().numpy()
+    ref = oracle_decode(c, mode="exact", p_mode=p_mode)
+    assert np.array_equal(bits(got), bits(ref))
+
+
+def test_paged_full_size_serving_m4_equals_contiguous():
+    # B = 64 sequences of 512..32768 keys, M = 4 (R = 32 rows per kv head),
+    # 64-row pages: about 8000 pages shuffled over the pool.
+    import torch
+    import int8_kv_decode_gb300 as K
+    wl = WORKLOADS["serving_b64_m4"]
+    x = make_workload(wl, device="cuda")
+    k8 = torch.empty((wl.Hkv, x.cap_rows, wl.d), dtype=torch.int8, device="cuda")
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((wl.Hkv, x.cap_rows), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    K.quantize_kv(x.k_rows, k8, ks)
+    K.quantize_kv(x.v_rows, v8, vs)
+    rs = torch.as_tensor(x.row_start, device="cuda")
+    ctx = torch.as_tensor(x.ctx, device="cuda")
+    q = torch.as_tensor(x.q, device="cuda")
+    ref = K.decode(q, k8, ks, v8, vs, rs, ctx, x.max_ctx)
+    L = page_layout(x.ctx, x.row_start, wl.M, 64, seed=11)
+    kp, ksp, vp, vsp = paged_copy(L, k8, ks, v8, vs, seed=11)
+    del k8, v8
+    bt = torch.from_numpy(L.block_table).cuda()
+    ws = K.alloc_workspace(wl.B, wl.M, wl.Hq, x.max_ctx)
+    got = K.decode_paged(q, kp, ksp, vp, vsp, bt, 64, ctx, x.max_ctx, workspace=ws)
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
+    assert K.get_device_status(ws) == 0
+
+
+def test_paged_bad_tables_are_flagged_without_touching_other_sequences():
+    import torch
+    import int8_kv_decode_gb300 as K
+    wl = custom("paged_bad", 6, 2, 8, 2, ("uniform", 100, 900), outliers=False)
+    c = upload(wl)
+    pc = Paged(c, 64, seed=3)
+    ws = K.alloc_workspace(wl.B, wl.M, wl.Hq, c.x.max_ctx)
+    clean = pc.decode(c, workspace=ws).cpu().numpy()
+    assert K.get_device_status(ws) == 0
+    n_pages = (c.x.ctx + wl.M - 1 + 63) // 64
+    # a table too narrow for the longest sequences: those get NaN rows
+    cols = int(np.median(n_pages))
+    narrow = pc.bt[:, :cols].contiguous()
+    out = pc.decode(c, bt=narrow, workspace=ws).cpu().numpy()
+    short = n_pages > cols
+    assert short.any() and (~short).any()
+    assert np.isnan(out[short]).all()
+    assert np.array_equal(bits(out[~short]), bits(clean[~short]))
+    assert K.get_device_status(ws) == 1          # KATTN_DEVERR_BAD_SEQUENCE
+    # entries outside the pool (one too large, one negative): flagged, page 0 read instead
+    bad = pc.bt.clone()
+    bad[1, 0] = pc.layout.n_pages + 5
+    bad[4, n_pages[4] - 1] = -3
+    out = pc.decode(c, bt=bad, workspace=ws).cpu().numpy()
+    others = [b for b in range(wl.B) if b not in (1, 4)]
+    assert np.array_equal(bits(out[others]), bits(clean[others]))
+    assert np.isfinite(out[[1, 4]]).all()
+    assert K.get_device_status(ws) == 4          # KATTN_DEVERR_BAD_PAGE
+    torch.cuda.synchronize()
