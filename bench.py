@@ -38,7 +38,7 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES_NOMINAL = 129 * 1024 * 1024
 HEAD_DIM = 128
-KERNEL_SOURCES = ["decode_fast.cu", "device_common.cuh", "kattn_internal.cuh"]
+KERNEL_SOURCES = ["decode_fast.cu", "decode_split.cuh", "device_common.cuh", "kattn_internal.cuh"]
 
 
 # ------------------------------------------------------------ accounting --
