@@ -69,6 +69,8 @@ enum kattn_p_mode {
 #define KATTN_HEAD_DIM 128 /* the only supported head_dim */
 #define KATTN_MAX_M 8      /* draft columns per sequence */
 #define KATTN_MAX_ROWS 64  /* g * M query rows per (sequence, kv head) */
+#define KATTN_WINDOW_KEYS 512 /* keys per window of the fast path's fixed tiling
+                                 (the unit of kattn_decode_shard's shards) */
 
 /* Device error bits reported by kattn_get_device_status. */
 #define KATTN_DEVERR_BAD_SEQUENCE 0x1u /* row_start / ctx_len out of range */
@@ -215,6 +217,60 @@ int kattn_decode_append(const float* q, const float* k_new, const float* v_new,
                         const int64_t* row_start, const int32_t* ctx_len, int B, int M, int Hq,
                         int Hkv, int d, int cap_rows, int max_ctx, float sm_scale, int p_mode,
                         float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------ context parallel -- */
+/* One sequence's keys spread over several GPUs (context parallelism): every
+ * GPU reduces the 512-key windows it holds into window partials, the
+ * partials are all-gathered, and kattn_merge_shards combines them in the
+ * same fixed order as kattn_decode.  Each window's partial is computed
+ * exactly as kattn_decode computes it, so the merged output equals, byte for
+ * byte, kattn_decode (fast mode) on one cache holding every key.  The pages
+ * fix only that the combine order must not depend on the batch
+ * ("Kestrel_VLLM - 18", §二); the window tiling is kattn_get_tiling's.
+ *
+ * Shards: windows are cut at absolute key positions, 512 keys each (window w
+ * holds keys [512w, 512w + 512) of a sequence's ctx_len + M - 1 keys).  Shard
+ * s holds windows [s*Ws, (s+1)*Ws) of EVERY sequence, Ws = win_per_shard; a
+ * merge needs n_shards*Ws >= ceil((ctx_len[b] + M - 1) / 512) for every b.
+ *
+ * Byte size of one shard's partials array, float32
+ * [B][Ws][Hkv][stride], stride = g*M*(d+2) rounded up to a multiple of 4
+ * (o[g*M][d], then m[g*M], then l[g*M]); 0 for invalid arguments. */
+size_t kattn_shard_partials_size(int B, int M, int Hq, int Hkv, int win_per_shard);
+
+/* The window partials of shard `shard` (fast mode).  This shard's cache holds
+ * key t of sequence b, for t in [512*shard*Ws, min(512*(shard+1)*Ws,
+ * ctx_len[b] + M - 1)), at row row_start[b] + t - 512*shard*Ws of every kv-head
+ * plane of k, v, k_scale, v_scale (shapes as kattn_decode); sequences with no
+ * key in the shard are skipped and row_start[b] is not read.  q, ctx_len
+ * (the GLOBAL context lengths), M, heads, max_ctx, sm_scale and p_mode are the
+ * same on every shard.  partials: float32 [B][Ws][Hkv][stride] (16-byte
+ * aligned): the partial of the shard's window w of (b, kh) at [b][w - shard*Ws][kh];
+ * entries for windows a sequence does not have are left untouched.
+ * workspace: kattn_decode_workspace_size(B, M, Hq, max_ctx) bytes, as for
+ * kattn_decode.  A sequence whose shard rows leave [0, cap_rows) or whose
+ * ctx_len is outside [1, max_ctx] gets o = NaN, m = +inf, l = NaN in every
+ * window of the shard, so its merged rows are NaN, and KATTN_DEVERR_BAD_SEQUENCE
+ * in this workspace's error word.  Errors as kattn_decode; exact mode and the
+ * paged layout are not offered here. */
+int kattn_decode_shard(const float* q, const int8_t* k, const float* k_scale, const int8_t* v,
+                       const float* v_scale, const int64_t* row_start, const int32_t* ctx_len,
+                       int B, int M, int Hq, int Hkv, int d, int cap_rows, int max_ctx, int shard,
+                       int win_per_shard, float sm_scale, int p_mode, float* partials,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Combination of the gathered partials into out: partials float32
+ * [n_shards][B][Ws][Hkv][stride] (shard-major, as an all-gather of the
+ * shards' arrays leaves them), ctx_len int32 [B] on the device, out float32
+ * [B][M][Hq][d].  Row (b, j, h) combines the windows of its own ctx_len[b] + j
+ * keys: m = max of the window maxima, weights e^(m_w - m), window sums in an
+ * order fixed by the window count alone, then out = o / l.  workspace: at
+ * least 256 bytes (only its error word is used; a decode workspace will do).
+ * A sequence with ctx_len outside [1, max_ctx], or with more windows than
+ * n_shards*Ws, gets NaN rows and KATTN_DEVERR_BAD_SEQUENCE. */
+int kattn_merge_shards(const float* partials, const int32_t* ctx_len, int B, int M, int Hq,
+                       int Hkv, int d, int max_ctx, int n_shards, int win_per_shard, float* out,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* Allocation-free form of kattn_decode in fast mode (exact_mode = 0).  The
  * pages have no counterpart to it: it exists for callers that cannot give the

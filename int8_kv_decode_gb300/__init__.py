@@ -6,17 +6,22 @@ in include/kattn.h); this package is a thin torch-facing binding.
 
 from .api import (  # noqa: F401
     P_MODES,
+    WINDOW_KEYS,
     alloc_workspace,
     decode,
     decode_append,
     decode_paged,
+    decode_shard,
     decode_workspace_size,
     expf_constants,
     get_device_status,
     get_tiling,
     hash_rows,
+    merge_shards,
+    partial_stride,
     qk_scores_debug,
     quantize_kv,
     quantize_kv_rows,
+    shard_partials_size,
 )
 from ._lib import KattnError, LIB_PATH, load  # noqa: F401

@@ -38,6 +38,13 @@ SIGNATURES = {
     "kattn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                      c_int, c_int, c_float, c_int, c_void_p, c_void_p]),
+    "kattn_shard_partials_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "kattn_decode_shard": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                   c_int, c_int, c_float, c_int, c_void_p, c_void_p, c_size_t,
+                                   c_void_p]),
+    "kattn_merge_shards": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                   c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "kattn_qk_scores_debug": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
                                       c_int, c_int, c_int, c_int, c_int, c_int, c_void_p,
                                       c_void_p, c_void_p, c_void_p]),

@@ -224,6 +224,93 @@ def decode_append(q, k_new, v_new, dst_rows, k, k_scale, v, v_scale, row_start, 
     return out
 
 
+WINDOW_KEYS = 512   # KATTN_WINDOW_KEYS: keys per window, the unit of a shard
+
+
+def shard_partials_size(B: int, M: int, Hq: int, Hkv: int, win_per_shard: int) -> int:
+    """Bytes of one shard's partials array (kattn_shard_partials_size)."""
+    return int(_lib.load().kattn_shard_partials_size(B, M, Hq, Hkv, win_per_shard))
+
+
+def partial_stride(R: int) -> int:
+    """Floats per (sequence, window, kv head) partial: o[R][128], m[R], l[R],
+    padded to a multiple of 4."""
+    return R * 128 + (2 * R + 3) // 4 * 4
+
+
+def decode_shard(q, k, k_scale, v, v_scale, row_start, ctx_len, max_ctx: int, shard: int,
+                 win_per_shard: int, *, partials=None, p_mode=0, sm_scale: float = 0.0,
+                 workspace=None):
+    """Window partials of context-parallel shard `shard` (kattn_decode_shard).
+
+    The cache k, v [Hkv][cap][d] (int8) and k_scale, v_scale [Hkv][cap] hold
+    key t of sequence b, for the shard's keys t in [512 * shard * Ws,
+    min(512 * (shard + 1) * Ws, ctx_len[b] + M - 1)), at row row_start[b] + t -
+    512 * shard * Ws; ctx_len holds the global context lengths.  Returns
+    partials float32 [B][Ws][Hkv][partial_stride(g * M)].
+    """
+    _need(q, torch.float32, "q", 4)
+    _need(k, torch.int8, "k", 3)
+    _need(v, torch.int8, "v", 3)
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(v_scale, torch.float32, "v_scale", 2)
+    _need(row_start, torch.int64, "row_start", 1)
+    _need(ctx_len, torch.int32, "ctx_len", 1)
+    B, M, Hq, d = q.shape
+    Hkv, cap, _ = k.shape
+    if tuple(v.shape) != tuple(k.shape) or tuple(k_scale.shape) != (Hkv, cap) \
+            or tuple(v_scale.shape) != (Hkv, cap):
+        raise ValueError("k/v/scales shapes disagree")
+    if row_start.numel() != B or ctx_len.numel() != B:
+        raise ValueError("row_start / ctx_len must have B entries")
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    stride = partial_stride(Hq // Hkv * M)
+    shape = (B, win_per_shard, Hkv, stride)
+    if partials is None:
+        partials = torch.empty(shape, dtype=torch.float32, device=q.device)
+    else:
+        _need(partials, torch.float32, "partials", 4)
+        if tuple(partials.shape) != shape:
+            raise ValueError(f"partials must have shape {shape}")
+    if workspace is None:
+        workspace = alloc_workspace(B, M, Hq, max_ctx, q.device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    mode = P_MODES.get(p_mode, p_mode) if isinstance(p_mode, str) else int(p_mode)
+    lib = _lib.load()
+    _lib.check("kattn_decode_shard", lib.kattn_decode_shard(
+        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(v), _ptr(v_scale), _ptr(row_start), _ptr(ctx_len),
+        B, M, Hq, Hkv, d, cap, int(max_ctx), int(shard), int(win_per_shard), float(sm_scale),
+        mode, _ptr(partials), _ptr(workspace), workspace.numel(), _stream(q.device)))
+    return partials
+
+
+def merge_shards(partials, ctx_len, M: int, Hq: int, max_ctx: int, *, out=None, workspace=None):
+    """Combine gathered shard partials [n_shards][B][Ws][Hkv][stride] into
+    out [B][M][Hq][128] float32 (kattn_merge_shards)."""
+    _need(partials, torch.float32, "partials", 5)
+    _need(ctx_len, torch.int32, "ctx_len", 1)
+    n_shards, B, Ws, Hkv, stride = partials.shape
+    if ctx_len.numel() != B:
+        raise ValueError("ctx_len must have B entries")
+    if Hq % Hkv != 0 or stride != partial_stride(Hq // Hkv * M):
+        raise ValueError("partials do not match M, Hq")
+    if out is None:
+        out = torch.empty((B, M, Hq, 128), dtype=torch.float32, device=partials.device)
+    else:
+        _need(out, torch.float32, "out", 4)
+        if tuple(out.shape) != (B, M, Hq, 128):
+            raise ValueError("out must have shape [B][M][Hq][128]")
+    if workspace is None:
+        workspace = torch.zeros(256, dtype=torch.uint8, device=partials.device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    lib = _lib.load()
+    _lib.check("kattn_merge_shards", lib.kattn_merge_shards(
+        _ptr(partials), _ptr(ctx_len), B, int(M), int(Hq), Hkv, 128, int(max_ctx), n_shards, Ws,
+        _ptr(out), _ptr(workspace), workspace.numel(), _stream(partials.device)))
+    return out
+
+
 def hash_rows(x: torch.Tensor) -> torch.Tensor:
     """FNV-1a 64 of every row of x (a CUDA tensor whose last dimension is
     contiguous; rows = all leading indices).  Returns int64 [rows] holding

@@ -51,7 +51,20 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodePa
         w = warp_quantize_row(p.q + orow, &s);
       } else {
         const float nan = __int_as_float(0x7fc00000);
-        reinterpret_cast<float4*>(p.out + orow)[lane] = make_float4(nan, nan, nan, nan);
+        if (p.shard_mode) {
+          // every window partial of the row: o = NaN, m = +inf, l = NaN, so
+          // that a merge over the gathered shards yields NaN for the row
+          for (int wl = 0; wl < p.part_ws; ++wl) {
+            float* part = p.partials + (((size_t)b * p.part_ws + wl) * p.Hkv + kh) * partial_stride(p.R);
+            reinterpret_cast<float4*>(part + (size_t)r * kD)[lane] = make_float4(nan, nan, nan, nan);
+            if (lane == 0) {
+              part[(size_t)p.R * kD + r] = INFINITY;
+              part[(size_t)p.R * kD + p.R + r] = nan;
+            }
+          }
+        } else {
+          reinterpret_cast<float4*>(p.out + orow)[lane] = make_float4(nan, nan, nan, nan);
+        }
         if (r == 0 && kh == 0 && lane == 0) atomicOr(p.err_word, KATTN_DEVERR_BAD_SEQUENCE);
       }
     }
@@ -70,7 +83,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodePa
   const bool fused = p.list_blocks > 0;
   int* pre = fused ? s_pre : p.prefix;
   auto items_of = [&](int b) -> int {
-    return sequence_valid(p, b) ? nsplit_for(p.ctx_len[b] + p.M - 1) * p.Hkv : 0;
+    return sequence_valid(p, b) ? local_windows(p, p.ctx_len[b]) * p.Hkv : 0;
   };
   const int per = (p.B + kThreads - 1) / kThreads;
   const int b_lo = min(p.B, tid * per), b_hi = min(p.B, b_lo + per);
@@ -111,7 +124,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prepare_kernel(const DecodePa
       else hi = mid;
     }
     const int i = j - s_pre[lo], w = i / p.Hkv, kh = i - w * p.Hkv;
-    p.items[j] = make_int4(lo | (kh << 16), w, kh * p.cap_rows + sequence_row0(p, lo),
+    p.items[j] = make_int4(lo | (kh << 16), p.win_begin + w, kh * p.cap_rows + sequence_row0(p, lo),
                            p.ctx_len[lo]);
   }
 }
@@ -153,7 +166,7 @@ __global__ void __launch_bounds__(kListThreads) list_kernel(const DecodeParams p
     const int first = crossed == 0 ? base : prev;
     if (j < total) {
       const int i = j - first, w = i / p.Hkv, kh = i - w * p.Hkv;
-      p.items[j] = make_int4(b | (kh << 16), w, kh * p.cap_rows + sequence_row0(p, b),
+      p.items[j] = make_int4(b | (kh << 16), p.win_begin + w, kh * p.cap_rows + sequence_row0(p, b),
                              p.ctx_len[b]);
     }
   }
@@ -187,17 +200,32 @@ merge_windows_kernel(const DecodeParams p) {
   const int row = WPR == 1 ? (int)blockIdx.x * kRowsPerCta + warp : (int)blockIdx.x;   // kh * R + r
   if (row >= p.Hkv * R) return;
   const int kh = row / R, r = row - kh * R;
-  if (!sequence_valid(p, b)) return;             // NaN rows already written
+  const int j = r / gq, h = kh * gq + (r - j * gq);
+  float4* dst = reinterpret_cast<float4*>(p.out + ((((int64_t)b * p.M + j) * p.Hq + h) * kD)) + lane;
+  if (!sequence_valid(p, b)) {                  // decode: NaN rows already written
+    if (p.merge_all && (WPR == 1 || warp == 0)) {
+      const float nan = __int_as_float(0x7fc00000);
+      *dst = make_float4(nan, nan, nan, nan);
+      if (r == 0 && kh == 0 && lane == 0) atomicOr(p.err_word, KATTN_DEVERR_BAD_SEQUENCE);
+    }
+    return;
+  }
   const int ctx = p.ctx_len[b];
-  if (nsplit_for(ctx + p.M - 1) == 1) return;   // written directly by the decode kernel
+  // a sequence of one window was written directly by the decode kernel
+  if (!p.merge_all && nsplit_for(ctx + p.M - 1) == 1) return;
   const int ns = nsplit_for(ctx + r / gq);      // the windows this row sees
   const int pst = partial_stride(R);
   const size_t sstride = (size_t)p.Hkv * pst;   // floats from one window to the next
-  const float* base = p.partials + ((size_t)b * p.nsplit_max * p.Hkv + kh) * pst;
+  const size_t shstride = (size_t)p.B * p.part_ws * sstride;   // and from one shard to the next
+  const float* base = p.partials + ((size_t)b * p.part_ws * p.Hkv + kh) * pst;
   const float* mcol = base + (size_t)R * kD + r;
   const float* lcol = mcol + R;
   const float* ocol = base + (size_t)r * kD + 4 * lane;
-  auto ldo = [&](int s) { return __ldcg(reinterpret_cast<const float4*>(ocol + (size_t)s * sstride)); };
+  auto woff = [&](int s) -> size_t {            // window s of the row
+    return p.n_shards == 1 ? (size_t)s * sstride
+                           : (size_t)(s / p.part_ws) * shstride + (size_t)(s % p.part_ws) * sstride;
+  };
+  auto ldo = [&](int s) { return __ldcg(reinterpret_cast<const float4*>(ocol + woff(s))); };
   auto fma4 = [](float w, float4 v, float4 acc) {
     return make_float4(__fmaf_rn(w, v.x, acc.x), __fmaf_rn(w, v.y, acc.y), __fmaf_rn(w, v.z, acc.z),
                        __fmaf_rn(w, v.w, acc.w));
@@ -214,10 +242,10 @@ merge_windows_kernel(const DecodeParams p) {
   if constexpr (WPR == 1) {
     // lane k: windows k and k + 32 (ns <= 64)
     const bool h0 = lane < ns, h1 = lane + kMergeSlots < ns;
-    const float m0 = h0 ? __ldcg(mcol + (size_t)lane * sstride) : -INFINITY;
-    const float m1 = h1 ? __ldcg(mcol + (size_t)(lane + kMergeSlots) * sstride) : -INFINITY;
-    const float l0 = h0 ? __ldcg(lcol + (size_t)lane * sstride) : 0.0f;
-    const float l1 = h1 ? __ldcg(lcol + (size_t)(lane + kMergeSlots) * sstride) : 0.0f;
+    const float m0 = h0 ? __ldcg(mcol + woff(lane)) : -INFINITY;
+    const float m1 = h1 ? __ldcg(mcol + woff(lane + kMergeSlots)) : -INFINITY;
+    const float l0 = h0 ? __ldcg(lcol + woff(lane)) : 0.0f;
+    const float l1 = h1 ? __ldcg(lcol + woff(lane + kMergeSlots)) : 0.0f;
     const float M = warp_max(fmaxf(m0, m1));
     const float w0 = h0 ? exp_diff(m0, M) : 0.0f, w1 = h1 ? exp_diff(m1, M) : 0.0f;
     L = warp_sum(h1 ? __fmaf_rn(w1, l1, __fmul_rn(w0, l0)) : __fmul_rn(w0, l0));
@@ -244,7 +272,7 @@ merge_windows_kernel(const DecodeParams p) {
   } else {
     // warp k = slot k: windows k, k + 32, ...
     float mloc = -INFINITY;
-    for (int s = warp; s < ns; s += kMergeSlots) mloc = fmaxf(mloc, __ldcg(mcol + (size_t)s * sstride));
+    for (int s = warp; s < ns; s += kMergeSlots) mloc = fmaxf(mloc, __ldcg(mcol + woff(s)));
     if (lane == 0) sm_red[warp] = mloc;
     __syncthreads();
     const float M = warp_max(sm_red[lane]);     // the 32 slot maxima (-inf for empty slots)
@@ -252,8 +280,8 @@ merge_windows_kernel(const DecodeParams p) {
     float il = 0.0f;
 #pragma unroll 4
     for (int s = warp; s < ns; s += kMergeSlots) {
-      const float w = exp_diff(__ldcg(mcol + (size_t)s * sstride), M);
-      const float ls = __ldcg(lcol + (size_t)s * sstride);
+      const float w = exp_diff(__ldcg(mcol + woff(s)), M);
+      const float ls = __ldcg(lcol + woff(s));
       const float4 v = ldo(s);
       if (s == warp) {
         in = mul4(w, v);
@@ -271,8 +299,6 @@ merge_windows_kernel(const DecodeParams p) {
     O = sm_o[0][lane];
     for (int k = 1; k < kMergeSlots && k < ns; ++k) O = add4(O, sm_o[k][lane]);
   }
-  const int j = r / gq, h = kh * gq + (r - j * gq);
-  float4* dst = reinterpret_cast<float4*>(p.out + ((((int64_t)b * p.M + j) * p.Hq + h) * kD)) + lane;
   *dst = make_float4(__fdiv_rn(O.x, L), __fdiv_rn(O.y, L), __fdiv_rn(O.z, L), __fdiv_rn(O.w, L));
 }
 
@@ -350,11 +376,18 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
   // 2. the split-KV pass
   e = p.block_table != nullptr ? launch_split_paged(p, maps, stream)
                                : launch_split_contiguous(p, maps, stream);
-  if (e != cudaSuccess || p.nsplit_max <= 1) return e;
-  // 3. the window merge (the same arithmetic in both shapes).  Estimated
-  //    time = waves x dependent loads per row: one warp per row (32 rows
-  //    per SM at once; a load round per 4 windows) or 32 warps per row (one
-  //    row per SM; a round per 128 windows), for rows of up to 64 windows.
+  if (e != cudaSuccess || p.nsplit_max <= 1 || p.shard_mode) return e;
+  // 3. the window merge
+  return launch_merge(p, stream);
+}
+
+// The window merge (the same arithmetic in both shapes), over the windows of
+// at most n_shards * part_ws per row.  Estimated time = waves x dependent
+// loads per row: one warp per row (32 rows per SM at once; a load round per 4
+// windows) or 32 warps per row (one row per SM; a round per 128 windows), for
+// rows of up to 64 windows.
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
+  const int nwin = p.n_shards * p.part_ws;
   const int rows_b = p.Hkv * p.R;                 // rows of one sequence
   const int64_t all_rows = (int64_t)rows_b * p.B;
   int sms = 0;
@@ -364,9 +397,9 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
       sms = 1;
   }
-  const int64_t est_warp = (all_rows + 32LL * sms - 1) / (32LL * sms) * ((p.nsplit_max + 3) / 4 + 2);
-  const int64_t est_cta = (all_rows + sms - 1) / sms * ((p.nsplit_max + 127) / 128 + 3);
-  if (p.nsplit_max <= 2 * kMergeSlots && est_warp <= est_cta)
+  const int64_t est_warp = (all_rows + 32LL * sms - 1) / (32LL * sms) * ((nwin + 3) / 4 + 2);
+  const int64_t est_cta = (all_rows + sms - 1) / sms * ((nwin + 127) / 128 + 3);
+  if (nwin <= 2 * kMergeSlots && est_warp <= est_cta)
     return launch_pdl(merge_windows_kernel<1>, dim3((unsigned)((rows_b + 7) / 8), (unsigned)p.B),
                       dim3(256), 0, stream, p);
   return launch_pdl(merge_windows_kernel<kMergeSlots>, dim3((unsigned)rows_b, (unsigned)p.B),

@@ -871,10 +871,11 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
               o[md][nr][u] = __fadd_rn(o[md][nr][u], other[((nr * 8 + md) * 4 + u) * 32 + lane]);
-        const bool whole = nsplit_for(ctx + M - 1) == 1;   // the sequence is one window
+        // the sequence is one window: out directly (shard mode: always a partial)
+        const bool whole = !p.shard_mode && nsplit_for(ctx + M - 1) == 1;
         const int kh = it0.kh, b = it0.b;
-        float* part = p.partials +
-                      (((size_t)b * p.nsplit_max + it0.w) * p.Hkv + kh) * partial_stride(R);
+        float* part = p.partials + (((size_t)b * p.part_ws + (it0.w - p.win_begin)) * p.Hkv + kh) *
+                                       partial_stride(R);
 #pragma unroll
         for (int nr = 0; nr < NR; ++nr)
 #pragma unroll

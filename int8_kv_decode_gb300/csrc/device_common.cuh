@@ -90,8 +90,22 @@ __device__ __forceinline__ bool sequence_ok(int64_t rs, int ctx, int M, int cap_
 // contiguous rows [row_start, row_start + ctx + M - 1), or the first
 // ceil((ctx + M - 1) / page) entries of its block-table row.  (The entries
 // themselves are checked where they are read: paged_row.)
+// In shard mode only the shard's keys must lie in the cache: the rows
+// [row_start, row_start + n) for the n keys of windows [win_begin, win_begin
+// + part_ws); a merge of shards checks ctx_len against the windows gathered.
 __device__ __forceinline__ bool sequence_valid(const DecodeParams& p, int b) {
   const int ctx = p.ctx_len[b];
+  if (p.merge_all)
+    return ctx >= 1 && ctx <= p.max_ctx &&
+           nsplit_for(ctx + p.M - 1) <= (int64_t)p.n_shards * p.part_ws;
+  if (p.shard_mode) {
+    if (ctx < 1 || ctx > p.max_ctx) return false;
+    const int64_t k0 = (int64_t)p.win_begin * kSplitC;
+    const int64_t k1 = min((int64_t)ctx + p.M - 1, k0 + (int64_t)p.part_ws * kSplitC);
+    if (k1 <= k0) return true;                    // no key of b in this shard
+    const int64_t rs = p.row_start[b];
+    return rs >= 0 && rs + (k1 - k0) <= (int64_t)p.cap_rows;
+  }
   if (p.block_table == nullptr) return sequence_ok(p.row_start[b], ctx, p.M, p.cap_rows, p.max_ctx);
   if (ctx < 1 || ctx > p.max_ctx) return false;
   const int64_t keys = (int64_t)ctx + p.M - 1;
@@ -111,9 +125,20 @@ __device__ __forceinline__ int paged_row(const DecodeParams& p, int b, int key) 
 }
 
 // Row of key 0 of sequence b within its plane: the contiguous layout's
-// row_start; 0 when paged (rows then come from paged_row).
+// row_start; 0 when paged (rows then come from paged_row).  In shard mode the
+// cache holds the shard's keys from row_start on, so key t sits at row
+// row_start + t - win_begin * kSplitC (this value may be negative; a key of
+// the shard never is).
 __device__ __forceinline__ int sequence_row0(const DecodeParams& p, int b) {
-  return p.block_table == nullptr ? (int)p.row_start[b] : 0;
+  if (p.block_table != nullptr) return 0;
+  return (int)p.row_start[b] - (p.shard_mode ? p.win_begin * kSplitC : 0);
+}
+
+// Windows of sequence b (ctx_len ctx) that this call reduces: all of them,
+// or in shard mode those of windows [win_begin, win_begin + part_ws).
+__device__ __forceinline__ int local_windows(const DecodeParams& p, int ctx) {
+  const int nw = nsplit_for(ctx + p.M - 1);
+  return p.shard_mode ? min(max(nw - p.win_begin, 0), p.part_ws) : nw;
 }
 
 // ------------------------------------------------------------ cp.async ----

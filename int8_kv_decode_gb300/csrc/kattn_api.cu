@@ -63,6 +63,8 @@ DecodeParams make_params(const float* q, const int8_t* k, const float* k_scale,
   p.cap_rows = cap_rows;
   p.max_ctx = max_ctx;
   p.nsplit_max = nsplit_for(max_ctx + M - 1);
+  p.part_ws = p.nsplit_max;
+  p.n_shards = 1;
   p.sm_scale = resolve_sm_scale(sm_scale, KATTN_HEAD_DIM);
   p.p_mode = p_mode;
   return p;
@@ -271,6 +273,83 @@ int kattn_qk_scores_debug(const float* q, const int8_t* k, const float* k_scale,
   DecodeParams p = make_params(q, k, k_scale, nullptr, nullptr, row_start, ctx_len, B, M, Hq,
                                Hkv, cap_rows, max_ctx, 0.0f, 0, nullptr);
   cudaError_t e = launch_qk_debug(p, scores, q_i8, q_scale, as_stream(stream));
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+}
+
+size_t kattn_shard_partials_size(int B, int M, int Hq, int Hkv, int win_per_shard) {
+  if (B < 1 || M < 1 || M > KATTN_MAX_M || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 ||
+      win_per_shard < 1)
+    return 0;
+  const int R = Hq / Hkv * M;
+  if (R > KATTN_MAX_ROWS) return 0;
+  return (size_t)B * (size_t)win_per_shard * (size_t)Hkv * (size_t)partial_stride(R) *
+         sizeof(float);
+}
+
+int kattn_decode_shard(const float* q, const int8_t* k, const float* k_scale, const int8_t* v,
+                       const float* v_scale, const int64_t* row_start, const int32_t* ctx_len,
+                       int B, int M, int Hq, int Hkv, int d, int cap_rows, int max_ctx, int shard,
+                       int win_per_shard, float sm_scale, int p_mode, float* partials,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_common(q, k, k_scale, row_start, 8, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
+  if (st != KATTN_OK) return st;
+  if (shard < 0 || win_per_shard < 1) return KATTN_ERR_INVALID_ARG;
+  // key positions of the shard are int32 on the device
+  if (((int64_t)shard + 1) * win_per_shard * kSplitC > (int64_t)INT32_MAX / 2)
+    return KATTN_ERR_INVALID_ARG;
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
+  if (B == 0) return KATTN_OK;
+  if (!v || !v_scale || !partials) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(v, 16) || !aligned(v_scale, 4) || !aligned(partials, 16))
+    return KATTN_ERR_MISALIGNED;
+  DecodeParams p = make_params(q, k, k_scale, v, v_scale, row_start, ctx_len, B, M, Hq, Hkv,
+                               cap_rows, max_ctx, sm_scale, p_mode, nullptr);
+  const WorkspaceLayout w = workspace_layout(B, M, Hq, max_ctx);
+  if ((int64_t)B * w.nsplit_max * Hkv > (int64_t)INT32_MAX / 4) return KATTN_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
+    return KATTN_ERR_WORKSPACE;
+  set_workspace(p, w, workspace);
+  p.partials = partials;                          // the caller's array, not the workspace's
+  p.shard_mode = 1;
+  p.win_begin = shard * win_per_shard;
+  p.part_ws = win_per_shard;
+  const cudaError_t e = launch_decode_fast(p, as_stream(stream));
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+}
+
+int kattn_merge_shards(const float* partials, const int32_t* ctx_len, int B, int M, int Hq,
+                       int Hkv, int d, int max_ctx, int n_shards, int win_per_shard, float* out,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || M < 1 || Hq < 1 || Hkv < 1 || max_ctx < 1 || n_shards < 1 || win_per_shard < 1)
+    return KATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || B > 65535 || Hkv > 65535) return KATTN_ERR_INVALID_ARG;
+  if (d != KATTN_HEAD_DIM) return KATTN_ERR_UNSUPPORTED;
+  if (M > KATTN_MAX_M || (Hq / Hkv) * M > KATTN_MAX_ROWS) return KATTN_ERR_UNSUPPORTED;
+  if ((int64_t)max_ctx + M - 1 > (int64_t)INT32_MAX / 2 ||
+      (int64_t)n_shards * win_per_shard > (int64_t)INT32_MAX / 2)
+    return KATTN_ERR_INVALID_ARG;
+  if (B == 0) return KATTN_OK;
+  if (!partials || !ctx_len || !out) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(partials, 16) || !aligned(ctx_len, 4) || !aligned(out, 16))
+    return KATTN_ERR_MISALIGNED;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256) return KATTN_ERR_WORKSPACE;
+  DecodeParams p{};
+  p.ctx_len = ctx_len;
+  p.out = out;
+  p.partials = const_cast<float*>(partials);
+  p.err_word = static_cast<uint32_t*>(workspace);
+  p.B = B;
+  p.M = M;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.g = Hq / Hkv;
+  p.R = p.g * M;
+  p.max_ctx = max_ctx;
+  p.part_ws = win_per_shard;
+  p.n_shards = n_shards;
+  p.merge_all = 1;
+  const cudaError_t e = launch_merge(p, as_stream(stream));
   return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
 }
 

@@ -22,6 +22,7 @@ constexpr int kSplitC = kSpanC * kSpansPerCta;   // 512 keys per CTA window
 constexpr int kMaxRows = KATTN_MAX_ROWS;
 constexpr int kMaxM = KATTN_MAX_M;
 static_assert(kSpanC % kBlockBk == 0, "a span is a whole number of blocks");
+static_assert(kSplitC == KATTN_WINDOW_KEYS, "the window of the public header");
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -106,6 +107,18 @@ struct DecodeParams {
   int cap_rows, max_ctx, nsplit_max;
   float sm_scale;       // already resolved (never 0)
   int p_mode;
+  // Window partials and context-parallel shards.  The partial of window w of
+  // (b, kv head kh) sits at float offset partial_stride(R) times
+  //   ((w / part_ws * B + b) * part_ws + w % part_ws) * Hkv + kh
+  // of partials: part_ws = nsplit_max and one shard for kattn_decode; for
+  // kattn_decode_shard / kattn_merge_shards, part_ws windows per sequence in
+  // each of n_shards shards, shard s holding windows [s * part_ws, (s + 1) * part_ws).
+  int part_ws;
+  int n_shards;
+  int win_begin;        // first window this call reduces (shard mode), else 0
+  int shard_mode;       // 1: write every window's partial and nothing of out
+  int merge_all;        // 1: merge every sequence (also single-window ones),
+                        //    validating ctx_len only (kattn_merge_shards)
 };
 
 // Constants of the table-driven exp used by exact mode; computed on the host
@@ -122,6 +135,7 @@ cudaError_t launch_quantize_kv(const float* x, int n_rows, int n_kv, int64_t row
                                int8_t* out_q, float* out_scale, int64_t dst_row0,
                                const int64_t* dst_rows, int cap_rows, cudaStream_t stream);
 cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_exact(const DecodeParams& p, const ExpfConsts& c,
                                 cudaStream_t stream);
 cudaError_t launch_hash_rows(const void* data, int64_t n_rows, int64_t row_bytes, int64_t stride,

@@ -156,3 +156,63 @@ def test_device_status_validation(lib):
     err = ctypes.c_int()
     assert lib.kattn_get_device_status(None, 1024, ctypes.byref(err), None) == -1
     assert lib.kattn_get_device_status(0x1010, 1024, ctypes.byref(err), None) == -4
+
+
+def _decode_shard(lib, **kw):
+    a = dict(q=64, k=64, ks=64, v=64, vs=64, rs=64, ctx=64, B=1, M=1, Hq=8, Hkv=2, d=128,
+             cap=256, max_ctx=2048, shard=0, ws_per=2, sm=0.0, p_mode=0, part=64, ws=0,
+             ws_bytes=0, stream=0)
+    a.update(kw)
+    return lib.kattn_decode_shard(a["q"], a["k"], a["ks"], a["v"], a["vs"], a["rs"], a["ctx"],
+                                  a["B"], a["M"], a["Hq"], a["Hkv"], a["d"], a["cap"],
+                                  a["max_ctx"], a["shard"], a["ws_per"], a["sm"], a["p_mode"],
+                                  a["part"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def _merge_shards(lib, **kw):
+    a = dict(part=64, ctx=64, B=1, M=1, Hq=8, Hkv=2, d=128, max_ctx=2048, n=2, ws_per=2,
+             out=64, ws=0x1000, ws_bytes=0, stream=0)
+    a.update(kw)
+    return lib.kattn_merge_shards(a["part"], a["ctx"], a["B"], a["M"], a["Hq"], a["Hkv"],
+                                  a["d"], a["max_ctx"], a["n"], a["ws_per"], a["out"], a["ws"],
+                                  a["ws_bytes"], a["stream"])
+
+
+def test_shard_validation(lib):
+    # Checked on the host before any CUDA call: the pointers are never used.
+    INVALID, UNSUP, MISAL, WS = -1, -2, -3, -4
+    assert _decode_shard(lib, shard=-1) == INVALID
+    assert _decode_shard(lib, ws_per=0) == INVALID
+    assert _decode_shard(lib, shard=1 << 20, ws_per=1 << 10) == INVALID   # keys beyond int32
+    assert _decode_shard(lib, part=0) == INVALID
+    assert _decode_shard(lib, part=0x1008) == MISAL
+    assert _decode_shard(lib, d=64) == UNSUP
+    assert _decode_shard(lib, p_mode=5) == INVALID
+    assert _decode_shard(lib, ws=0) == WS
+    assert _decode_shard(lib, B=0) == 0
+    assert _merge_shards(lib, n=0) == INVALID
+    assert _merge_shards(lib, ws_per=0) == INVALID
+    assert _merge_shards(lib, d=64) == UNSUP
+    assert _merge_shards(lib, M=9) == UNSUP
+    assert _merge_shards(lib, part=0x1004) == MISAL
+    assert _merge_shards(lib, out=0) == INVALID
+    assert _merge_shards(lib, ws=0x1000, ws_bytes=128) == WS               # < 256 bytes
+    assert _merge_shards(lib, ws=0x1010, ws_bytes=256) == WS               # not 256-aligned
+    assert _merge_shards(lib, B=0) == 0
+
+
+def test_shard_partials_size(lib):
+    # [B][Ws][Hkv][stride] float32, stride = R*128 + (2R rounded up to 4)
+    assert lib.kattn_shard_partials_size(3, 1, 8, 2, 5) == 3 * 5 * 2 * (4 * 128 + 8) * 4
+    assert lib.kattn_shard_partials_size(2, 5, 32, 4, 1) == 2 * 4 * (40 * 128 + 80) * 4
+    assert lib.kattn_shard_partials_size(2, 9, 32, 4, 1) == 0
+    assert lib.kattn_shard_partials_size(2, 1, 6, 4, 1) == 0
+    from int8_kv_decode_gb300 import api
+    assert api.partial_stride(40) == 40 * 128 + 80
+    assert api.partial_stride(3) == 3 * 128 + 8
+
+
+def test_window_constant_matches_header():
+    from int8_kv_decode_gb300 import api
+    text = open(HEADER, encoding="utf-8").read()
+    assert int(re.search(r"#define KATTN_WINDOW_KEYS (\d+)", text).group(1)) == api.WINDOW_KEYS
