@@ -54,11 +54,14 @@ def qo_bytes(B: int, M: int, Hq: int, d: int = HEAD_DIM) -> int:
     return 2 * B * M * Hq * d * 4
 
 
-def decode_launches(max_ctx: int, M: int, B: int) -> int:
-    """Kernels one fast-mode kattn_decode (or kattn_decode_append) launches:
-    query packing (with the append and, up to 2048 sequences, the work list),
-    the work list above 2048 sequences, the split-KV pass, and the window
-    merge when the longest row spans more than one 512-key window."""
+def decode_launches(max_ctx: int, M: int, B: int, exact: bool = False) -> int:
+    """Kernels one step launches.  Fast mode, kattn_decode_append: query
+    packing (with the append and, up to 2048 sequences, the work list), the
+    work list above 2048 sequences, the split-KV pass, and the window merge
+    when the longest row spans more than one 512-key window.  Exact mode: the
+    two appends (K and V) and the one exact-mode kernel."""
+    if exact:
+        return 3
     return 2 + (B > 2048) + (int(max_ctx) + M - 1 > 512)
 
 
@@ -316,11 +319,11 @@ def run_reference(args):
     return 0
 
 
-def workload_config(wl, ctx, note=None, l2=None, launch=None):
+def workload_config(wl, ctx, note=None, l2=None, launch=None, p_mode="f32", exact=False):
     import numpy as np
     c = {"workload": wl.name, "B": wl.B, "M": wl.M, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
          "ctx": wl.ctx if isinstance(wl.ctx, int) else f"{wl.ctx[0]}[{wl.ctx[1]},{wl.ctx[2]}]",
-         "mean_ctx": float(np.mean(ctx)), "p_mode": "f32", "exact_mode": False}
+         "mean_ctx": float(np.mean(ctx)), "p_mode": p_mode, "exact_mode": bool(exact)}
     if l2:
         c["l2"] = l2
     if launch:
@@ -380,15 +383,25 @@ def run_ours(args):
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
 
+    pm = K.P_MODES[args.p_mode]
+    exact = bool(args.exact)
+
     def decode(i):
         k8, ks, v8, vs = caches[i % n_copies]
-        K.decode(q, k8, ks, v8, vs, rs, ctx, max_ctx, out=out, workspace=ws)
+        K.decode(q, k8, ks, v8, vs, rs, ctx, max_ctx, out=out, workspace=None if exact else ws,
+                 p_mode=pm, exact_mode=exact)
 
     def step(i):
-        # this step's K/V rows appended inside the decode call
         k8, ks, v8, vs = caches[i % n_copies]
+        if exact:
+            # exact mode has no fused append: the two appends, then the decode
+            K.quantize_kv_rows(knew, dst, k8, ks)
+            K.quantize_kv_rows(vnew, dst, v8, vs)
+            decode(i)
+            return
+        # this step's K/V rows appended inside the decode call
         K.decode_append(q, knew, vnew, dst, k8, ks, v8, vs, rs, ctx, max_ctx, out=out,
-                        workspace=ws)
+                        workspace=ws, p_mode=pm)
 
     for i in range(args.warmup):
         step(i)
@@ -525,18 +538,20 @@ def run_ours(args):
         "config": workload_config(
             wl, x.ctx, l2=(f"inputs larger than L2: {kvb / 1e9:.2f} GB KV per step x "
                            f"{n_copies} rotating cache copies vs {l2 / 2**20:.0f} MiB L2"),
-            launch="eager" if args.no_graphs else "one CUDA graph replay per step"),
+            launch="eager" if args.no_graphs else "one CUDA graph replay per step",
+            p_mode=args.p_mode, exact=exact),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
                      "traffic": profiled_traffic(wl.name, sha),
-                     "kernel": "decode_fast_kernel", "algorithmic_bytes_per_launch": algo,
+                     "kernel": "decode_exact_kernel" if exact else "decode_fast_kernel",
+                     "algorithmic_bytes_per_launch": algo,
                      "avg_launch_us": decode_s * 1e6, "kernel_source_sha": sha},
         "kv_frac_of_step": (kvb / (elapsed / args.steps) / 1e9) / peak,
         "cpu_baseline": cpu,
         "e2e": {"value": total_bytes / e_tmax / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": decode_launches(max_ctx, M, B) * args.steps,
+        "gpu_launches": decode_launches(max_ctx, M, B, exact) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -557,6 +572,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cpu-all-cores", action="store_true",
                     help="skip the all-cores oracle baseline (the single-threaded one stays)")
+    ap.add_argument("--p-mode", default="f32", choices=["f32", "bf16", "e4m3", "e4m3x448",
+                                                        "e4m3x256"],
+                    help="rounding of the P that multiplies V")
+    ap.add_argument("--exact", action="store_true",
+                    help="time exact mode (token-order scan, table-driven exp) instead of fast mode")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every step eagerly instead of replaying CUDA graphs")
     ap.add_argument("--ref-sequences", type=int, default=2,

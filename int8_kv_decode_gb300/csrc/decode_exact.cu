@@ -11,13 +11,24 @@
 // Only the l and o chains are inherently serial.  The scores, the running
 // max (a prefix max, which is exact in any order) and every exp are computed
 // in parallel per chunk of 128 keys; then thread i walks channel i's chain
-// through the chunk.  One CTA of 128 threads per query row.
+// through the chunk, reading the chunk's V rows from shared memory.  One CTA
+// of 128 threads per query row.
 #include "device_common.cuh"
 
 namespace kattn {
 namespace {
 
 constexpr int kChunk = 128;
+constexpr int kSub = 32;                          // keys per step of the serial scan
+
+// f32 of a signed byte, exactly: the offset-binary byte u = v + 128 placed in
+// the low mantissa bits of 1.5 * 2^23 gives 12582912 + u; subtracting
+// 12582912 + 128 leaves v (both operands and the difference are integers
+// below 2^24, so nothing rounds).
+__device__ __forceinline__ float i8_to_f32(uint8_t byte) {
+  const uint32_t u = (uint32_t)(byte ^ 0x80u);
+  return __fsub_rn(__uint_as_float(0x4B400000u | u), 12583040.0f);
+}
 
 // Table-driven float32 exp (P. T. P. Tang, ACM TOMS 1989; the variant the
 // page describes in §3.3): x = (64m + j + r/C2)/K, exp(x) = 2^m 2^(j/64) e^r,
@@ -48,14 +59,25 @@ __device__ __forceinline__ float round_p_exact(float p, int mode) {
   }
 }
 
+// Shared memory of one row's CTA.  A chunk's K and V rows are staged by
+// cp.async one chunk ahead (two stages), so the serial scan reads V from
+// shared memory; the 16-byte pieces of a K row are placed at piece c ^ (key & 7)
+// so that the per-key dot products read without bank conflicts.
+struct ExactSmem {
+  int8_t k[2][kChunk][kD];
+  int8_t v[2][kChunk][kD];
+  float4 tok[kChunk];                             // per key: round_p(p), v_scale, alpha, p
+  ExpfConsts c;
+  int row[2][kChunk];                             // plane rows of the stage's keys
+  uint32_t q8[kD / 4];
+  float red[kChunk / 32];
+  float carry;
+};
+
 __global__ void __launch_bounds__(kChunk)
 decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
-  __shared__ ExpfConsts c;
-  __shared__ __align__(16) uint32_t q8[kD / 4];
-  __shared__ float red[kChunk / 32];
-  __shared__ float s_alpha[kChunk], s_p[kChunk], s_pr[kChunk], s_vs[kChunk];
-  __shared__ float s_carry;
-  __shared__ int s_row[kChunk];                   // plane rows of the chunk's keys
+  extern __shared__ __align__(16) unsigned char exact_smem[];
+  ExactSmem& sm = *reinterpret_cast<ExactSmem*>(exact_smem);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -74,18 +96,7 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   const int rs = sequence_row0(p, b);
 
   for (int i = tid; i < (int)(sizeof(ExpfConsts) / sizeof(double)); i += kChunk)
-    reinterpret_cast<double*>(&c)[i] = reinterpret_cast<const double*>(&consts)[i];
-
-  // int8 query: absmax over the 128 channels, then one IEEE division each.
-  const float x = p.q[qrow * kD + tid];
-  float amax = warp_max(fabsf(x));
-  if (lane == 0) red[warp] = amax;
-  __syncthreads();
-  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  const float qs = quant_scale(amax);
-  reinterpret_cast<int8_t*>(q8)[tid] = (int8_t)quant_one(x, qs);
-  if (tid == 0) s_carry = -INFINITY;
-  __syncthreads();
+    reinterpret_cast<double*>(&sm.c)[i] = reinterpret_cast<const double*>(&consts)[i];
 
   // Key t is row `row` of head kh's plane: rs + t, or from the block table.
   const int64_t plane = (int64_t)kh * p.cap_rows;
@@ -94,25 +105,77 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   const float* ksb = p.k_scale + plane;
   const float* vsb = p.v_scale + plane;
 
+  // The plane rows of the chunk at t0 (thread = key) and their scales.
+  float ks_next = 0.0f, vs_next = 0.0f;
+  auto stage_rows = [&](int t0, int st) {
+    const int t = t0 + tid;
+    int row = -1;
+    if (t < L) {
+      row = p.block_table == nullptr ? rs + t : paged_row(p, b, t);
+      ks_next = ksb[row];
+      vs_next = vsb[row];
+    }
+    sm.row[st][tid] = row;
+  };
+  // The copies of that chunk's K and V rows (after a barrier publishes the
+  // rows): 128 rows x 8 pieces of 16 bytes each, 8 pieces per thread.
+  auto issue = [&](int t0, int st) {
+    const int n = min(kChunk, L - t0);
+#pragma unroll
+    for (int i = 0; i < kD / 16; ++i) {
+      const int idx = i * kChunk + tid;
+      const int u = idx >> 3, c16 = idx & 7;
+      if (u < n) {
+        const int64_t off = (int64_t)sm.row[st][u] * kD + c16 * 16;
+        cp_async16(&sm.k[st][u][(c16 ^ (u & 7)) * 16], kbase + off, 16);
+        cp_async16(&sm.v[st][u][c16 * 16], vbase + off, 16);
+      }
+    }
+    cp_async_commit();
+  };
+
+  stage_rows(0, 0);
+  __syncthreads();
+  issue(0, 0);
+
+  // int8 query: absmax over the 128 channels, then one IEEE division each.
+  const float x = p.q[qrow * kD + tid];
+  float amax = warp_max(fabsf(x));
+  if (lane == 0) sm.red[warp] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(sm.red[0], sm.red[1]), fmaxf(sm.red[2], sm.red[3]));
+  const float qs = quant_scale(amax);
+  reinterpret_cast<int8_t*>(sm.q8)[tid] = (int8_t)quant_one(x, qs);
+  if (tid == 0) sm.carry = -INFINITY;
+  __syncthreads();
+
   float o = 0.0f, l = 0.0f;
-  for (int t0 = 0; t0 < L; t0 += kChunk) {
+  for (int t0 = 0, st = 0; t0 < L; t0 += kChunk, st ^= 1) {
     const int t = t0 + tid;
     const bool live = t < L;
+    const int n = min(kChunk, L - t0);
+    const float ks_cur = ks_next, vs_cur = vs_next;
+    // next chunk's rows and copies, in flight during this chunk
+    if (t0 + kChunk < L) stage_rows(t0 + kChunk, st ^ 1);
+    __syncthreads();
+    if (t0 + kChunk < L) issue(t0 + kChunk, st ^ 1);
+    else cp_async_commit();                       // an empty group keeps the count
+    cp_async_wait<1>();                           // this chunk's copies (own) landed
+    __syncthreads();                              // ... and everyone's
+
     float s = -INFINITY;
-    const int row = !live ? 0 : p.block_table == nullptr ? rs + t : paged_row(p, b, t);
-    s_row[tid] = row;
     if (live) {
-      const int4* krow = reinterpret_cast<const int4*>(kbase + (int64_t)row * kD);
+      const int4* krow = reinterpret_cast<const int4*>(sm.k[st][tid]);
       int acc = 0;
 #pragma unroll
       for (int cc = 0; cc < kD / 16; ++cc) {
-        const int4 kv = krow[cc];
-        acc = __dp4a((int)kv.x, (int)q8[4 * cc + 0], acc);
-        acc = __dp4a((int)kv.y, (int)q8[4 * cc + 1], acc);
-        acc = __dp4a((int)kv.z, (int)q8[4 * cc + 2], acc);
-        acc = __dp4a((int)kv.w, (int)q8[4 * cc + 3], acc);
+        const int4 kv = krow[cc ^ (tid & 7)];
+        acc = __dp4a((int)kv.x, (int)sm.q8[4 * cc + 0], acc);
+        acc = __dp4a((int)kv.y, (int)sm.q8[4 * cc + 1], acc);
+        acc = __dp4a((int)kv.z, (int)sm.q8[4 * cc + 2], acc);
+        acc = __dp4a((int)kv.w, (int)sm.q8[4 * cc + 3], acc);
       }
-      s = __fmul_rn(__fmul_rn((float)acc, __fmul_rn(qs, ksb[row])), p.sm_scale);
+      s = __fmul_rn(__fmul_rn((float)acc, __fmul_rn(qs, ks_cur)), p.sm_scale);
     }
     // Inclusive prefix max over the chunk, seeded with the running max.
     float pm = s;
@@ -121,35 +184,54 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
       const float o2 = __shfl_up_sync(0xffffffffu, pm, off);
       if (lane >= off) pm = fmaxf(pm, o2);
     }
-    if (lane == 31) red[warp] = pm;
-    const float carry = s_carry;
+    if (lane == 31) sm.red[warp] = pm;
+    const float carry = sm.carry;
     __syncthreads();
-    for (int w = 0; w < warp; ++w) pm = fmaxf(pm, red[w]);
+    for (int w = 0; w < warp; ++w) pm = fmaxf(pm, sm.red[w]);
     pm = fmaxf(pm, carry);
     // Running max before this key: the previous lane's inclusive max, or for
     // a warp's first lane the max of the carry and all earlier warps.
     float prev = __shfl_up_sync(0xffffffffu, pm, 1);
     if (lane == 0) {
       float pw = carry;
-      for (int w = 0; w < warp; ++w) pw = fmaxf(pw, red[w]);
+      for (int w = 0; w < warp; ++w) pw = fmaxf(pw, sm.red[w]);
       prev = pw;
     }
     if (live) {
-      const float a = expf_tang(__fsub_rn(prev, pm), c);
-      const float pp = expf_tang(__fsub_rn(s, pm), c);
-      s_alpha[tid] = a;
-      s_p[tid] = pp;
-      s_pr[tid] = round_p_exact(pp, p.p_mode);
-      s_vs[tid] = vsb[row];
+      const float a = expf_tang(__fsub_rn(prev, pm), sm.c);
+      const float pp = expf_tang(__fsub_rn(s, pm), sm.c);
+      sm.tok[tid] = make_float4(round_p_exact(pp, p.p_mode), vs_cur, a, pp);
     }
     __syncthreads();
-    if (tid == min(kChunk, L - t0) - 1) s_carry = pm;
-    const int n = min(kChunk, L - t0);
-    for (int u = 0; u < n; ++u) {
-      const float a = s_alpha[u];
-      const float vdeq = __fmul_rn((float)vbase[(int64_t)s_row[u] * kD + tid], s_vs[u]);
-      o = __fadd_rn(__fmul_rn(o, a), __fmul_rn(s_pr[u], vdeq));
-      l = __fadd_rn(__fmul_rn(l, a), s_p[u]);
+    if (tid == n - 1) sm.carry = pm;
+    // 32 keys at a time: first every key's term round_p(p) * (f32(v8) * vs)
+    // (independent of one another), then the two chains, key by key.
+    const uint8_t* vcol = reinterpret_cast<const uint8_t*>(&sm.v[st][0][tid]);
+    const float2* tk2 = reinterpret_cast<const float2*>(sm.tok);
+    for (int u0 = 0; u0 < n; u0 += kSub) {
+      float term[kSub];
+#pragma unroll
+      for (int i = 0; i < kSub; ++i) {
+        const float2 pv = tk2[2 * (u0 + i)];      // round_p(p), v_scale
+        term[i] = __fmul_rn(pv.x, __fmul_rn(i8_to_f32(vcol[(u0 + i) * kD]), pv.y));
+      }
+      if (u0 + kSub <= n) {
+#pragma unroll
+        for (int i = 0; i < kSub; ++i) {
+          const float2 ap = tk2[2 * (u0 + i) + 1];   // alpha, p
+          o = __fadd_rn(__fmul_rn(o, ap.x), term[i]);
+          l = __fadd_rn(__fmul_rn(l, ap.x), ap.y);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kSub; ++i) {
+          if (u0 + i < n) {
+            const float2 ap = tk2[2 * (u0 + i) + 1];
+            o = __fadd_rn(__fmul_rn(o, ap.x), term[i]);
+            l = __fadd_rn(__fmul_rn(l, ap.x), ap.y);
+          }
+        }
+      }
     }
     __syncthreads();
   }
@@ -161,7 +243,11 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
 cudaError_t launch_decode_exact(const DecodeParams& p, const ExpfConsts& c,
                                 cudaStream_t stream) {
   const int64_t rows = (int64_t)p.B * p.M * p.Hq;
-  decode_exact_kernel<<<(unsigned)rows, kChunk, 0, stream>>>(p, c);
+  const int smem = (int)sizeof(ExactSmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_exact_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  decode_exact_kernel<<<(unsigned)rows, kChunk, smem, stream>>>(p, c);
   return cudaGetLastError();
 }
 
