@@ -54,17 +54,6 @@ def qo_bytes(B: int, M: int, Hq: int, d: int = HEAD_DIM) -> int:
     return 2 * B * M * Hq * d * 4
 
 
-def decode_launches(max_ctx: int, M: int, B: int, exact: bool = False) -> int:
-    """Kernels one step launches.  Fast mode, kattn_decode_append: query
-    packing (with the append and, up to 2048 sequences, the work list), the
-    work list above 2048 sequences, the split-KV pass, and the window merge
-    when the longest row spans more than one 512-key window.  Exact mode: the
-    two appends (K and V) and the one exact-mode kernel."""
-    if exact:
-        return 3
-    return 2 + (B > 2048) + (int(max_ctx) + M - 1 > 512)
-
-
 def append_rows(row_start, ctx, M: int):
     """Cache rows written by this step: the M newest rows of each sequence
     (draft column j's own key is row ctx + j - 1)."""
@@ -551,7 +540,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": total_bytes / e_tmax / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": decode_launches(max_ctx, M, B, exact) * args.steps,
+        "gpu_launches": (3 if exact else K.decode_launch_count(B, M, Hq, Hkv, max_ctx)) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

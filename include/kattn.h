@@ -105,6 +105,13 @@ int kattn_get_tiling(int* split_C, int* round_block_Bk);
  * overlap on the GPU race and give undefined results. */
 size_t kattn_decode_workspace_size(int B, int M, int Hq, int max_ctx);
 
+/* Kernels one fast-mode kattn_decode or kattn_decode_append call launches for
+ * these sizes: the query packing (with the append and, up to 2048 sequences,
+ * the work list), the work list above 2048 sequences, the split-KV pass, and
+ * the window merge when max_ctx + M - 1 spans more than one 512-key window.
+ * 0 for invalid sizes. */
+int kattn_decode_launch_count(int B, int M, int Hq, int Hkv, int max_ctx);
+
 /* Quantize K or V rows into the int8 cache ("Kestrel_VLLM - 18" §四 fields
  * _k/_ks, _v/_vs).  For each row r < n_rows and kv head h < n_kv:
  *   scale = f32(max_i |x[r][h][i]|) / 127                (IEEE division)

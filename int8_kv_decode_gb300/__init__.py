@@ -10,6 +10,7 @@ from .api import (  # noqa: F401
     alloc_workspace,
     decode,
     decode_append,
+    decode_launch_count,
     decode_paged,
     decode_shard,
     decode_workspace_size,

@@ -20,6 +20,7 @@ SIGNATURES = {
     "kattn_status_string": (ctypes.c_char_p, [c_int]),
     "kattn_get_tiling": (c_int, [ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
     "kattn_decode_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
+    "kattn_decode_launch_count": (c_int, [c_int, c_int, c_int, c_int, c_int]),
     "kattn_quantize_kv": (c_int, [c_void_p, c_int, c_int, c_int, c_int64, c_void_p, c_void_p,
                                   c_int64, c_int, c_void_p]),
     "kattn_quantize_kv_rows": (c_int, [c_void_p, c_int, c_int, c_int, c_int64, c_void_p,

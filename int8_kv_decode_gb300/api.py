@@ -56,6 +56,12 @@ def decode_workspace_size(B: int, M: int, Hq: int, max_ctx: int) -> int:
     return int(_lib.load().kattn_decode_workspace_size(B, M, Hq, max_ctx))
 
 
+def decode_launch_count(B: int, M: int, Hq: int, Hkv: int, max_ctx: int) -> int:
+    """Kernels one fast-mode decode launches for these sizes on the current
+    device (kattn_decode_launch_count)."""
+    return int(_lib.load().kattn_decode_launch_count(B, M, Hq, Hkv, max_ctx))
+
+
 def alloc_workspace(B: int, M: int, Hq: int, max_ctx: int, device="cuda") -> torch.Tensor:
     """A zeroed workspace for kattn_decode (allocated by torch, not the library)."""
     n = decode_workspace_size(B, M, Hq, max_ctx)

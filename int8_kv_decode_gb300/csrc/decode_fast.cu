@@ -344,6 +344,11 @@ cudaError_t launch_split_contiguous(const DecodeParams& p, const TmaMaps& maps,
 
 }  // namespace
 
+int decode_launch_count(const DecodeParams& p) {
+  const bool merge = p.nsplit_max > 1 && !p.shard_mode;
+  return 2 + (p.B > kFusedListMaxB ? 1 : 0) + (merge ? 1 : 0);
+}
+
 cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
   TmaMaps maps;
   const int64_t rows = (int64_t)p.Hkv * p.cap_rows;

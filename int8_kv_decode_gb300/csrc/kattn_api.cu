@@ -276,6 +276,15 @@ int kattn_qk_scores_debug(const float* q, const int8_t* k, const float* k_scale,
   return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
 }
 
+int kattn_decode_launch_count(int B, int M, int Hq, int Hkv, int max_ctx) {
+  if (B < 1 || M < 1 || M > KATTN_MAX_M || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_ctx < 1 ||
+      (Hq / Hkv) * M > KATTN_MAX_ROWS || (int64_t)max_ctx + M - 1 > (int64_t)INT32_MAX / 2)
+    return 0;
+  const DecodeParams p = make_params(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                     nullptr, B, M, Hq, Hkv, 1, max_ctx, 0.0f, 0, nullptr);
+  return decode_launch_count(p);
+}
+
 size_t kattn_shard_partials_size(int B, int M, int Hq, int Hkv, int win_per_shard) {
   if (B < 1 || M < 1 || M > KATTN_MAX_M || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 ||
       win_per_shard < 1)

@@ -136,6 +136,7 @@ cudaError_t launch_quantize_kv(const float* x, int n_rows, int n_kv, int64_t row
                                const int64_t* dst_rows, int cap_rows, cudaStream_t stream);
 cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
+int decode_launch_count(const DecodeParams& p);   // kernels launch_decode_fast launches
 cudaError_t launch_decode_exact(const DecodeParams& p, const ExpfConsts& c,
                                 cudaStream_t stream);
 cudaError_t launch_hash_rows(const void* data, int64_t n_rows, int64_t row_bytes, int64_t stride,

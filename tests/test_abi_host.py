@@ -216,3 +216,13 @@ def test_window_constant_matches_header():
     from int8_kv_decode_gb300 import api
     text = open(HEADER, encoding="utf-8").read()
     assert int(re.search(r"#define KATTN_WINDOW_KEYS (\d+)", text).group(1)) == api.WINDOW_KEYS
+
+
+def test_launch_count_validation(lib):
+    f = lib.kattn_decode_launch_count
+    assert f(0, 1, 32, 4, 1024) == 0          # no sequences
+    assert f(4, 9, 32, 4, 1024) == 0          # M > KATTN_MAX_M
+    assert f(4, 1, 30, 4, 1024) == 0          # Hq not a multiple of Hkv
+    assert f(4, 1, 32, 4, 0) == 0
+    assert f(1, 1, 8, 2, 256) == 2            # one window: packing + split pass, no merge
+    assert f(4096, 1, 32, 4, 8192) == 4       # work list launch and merge launch

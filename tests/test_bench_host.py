@@ -92,12 +92,3 @@ def test_all_cores_oracle_baseline_runs_in_spawned_processes():
     from synth import WORKLOADS
     gbs, cores, secs = bench.time_oracle_all_cores(WORKLOADS["tiny"], 0.2)
     assert cores >= 1 and secs >= 0.2 and gbs > 0
-
-
-def test_launch_count_claims():
-    # fast: packing (+ list above 2048 sequences) + split pass (+ merge past one window)
-    assert bench.decode_launches(256, 1, 1) == 2
-    assert bench.decode_launches(1024, 1, 4) == 3
-    assert bench.decode_launches(1024, 1, 4096) == 4
-    # exact: two appends and the exact-mode kernel
-    assert bench.decode_launches(1024, 5, 16, exact=True) == 3

@@ -424,3 +424,25 @@ def test_row_hashes_match_the_oracle_and_find_a_planted_divergence():
     view = ex.reshape(-1, 128)[:, 1:101]
     assert np.array_equal(K.hash_rows(view).cpu().numpy().view(np.uint64),
                           H.hash_rows(ex.reshape(-1, 128)[:, 1:101].cpu().numpy()))
+
+
+@pytest.mark.parametrize("p_mode", [0, 2])
+def test_long_rows_alone_equal_the_batch(p_mode):
+    # Rows of up to 79 windows (several per merge slot), decoded in a batch
+    # of 40 and in sub-batches of one and three sequences: the same bytes,
+    # whichever launch shape the merge takes for each.
+    import int8_kv_decode_gb300 as K
+    wl = custom("long_mix", 40, 1, 32, 4, ("uniform", 600, 40000), outliers=True)
+    c = upload(wl)
+    assert K.decode_launch_count(40, 1, 32, 4, c.x.max_ctx) == 3
+    ws = K.alloc_workspace(40, 1, 32, c.x.max_ctx)
+    full = run(c, p_mode=p_mode, workspace=ws).cpu().numpy()
+    assert K.get_device_status(ws) == 0
+    for lo, hi in ((0, 1), (7, 10), (int(np.argmax(c.x.ctx)), int(np.argmax(c.x.ctx)) + 1)):
+        mc = int(c.x.ctx[lo:hi].max())
+        sub = K.decode(c.q[lo:hi].contiguous(), c.k8, c.ks, c.v8, c.vs, c.rs[lo:hi].contiguous(),
+                       c.ctx[lo:hi].contiguous(), mc, p_mode=p_mode).cpu().numpy()
+        assert np.array_equal(bits(full[lo:hi]), bits(sub)), (lo, hi)
+    rows = sample_rows(c.x, 24, seed=5)
+    if p_mode == 0:
+        assert_f32_tolerance(full, oracle_decode(c, rows=rows), row_mask(full.shape, rows))
