@@ -1,0 +1,60 @@
+"""How the rounded-P error behaves with context length on the GPU path.
+
+The susun-blog page (section "注意力权重") finds that P rounded straight to
+e4m3 degrades as the context grows. Its explanation is underflow: weights
+below about 0.001 of the running max become 0, and the rounding only ever
+loses mass. Its naive kernel rounds exp(s - m) against one running max over
+the whole row. The fast path here rounds against the running max of each
+128-key span (the split-KV tiling), and the spans are merged with f32 weights.
+So a longer context does not push more of a span's weights under the e4m3
+threshold. These tests pin that property on logits spread wide enough for
+underflow to matter (queries scaled by 5, no outlier channels):
+
+- the error of every fp8 mode against f32 P does not grow from 2.5k to 32k keys;
+- the output is not shrunk toward zero: the projection coefficient
+  <out, out_f32> / <out_f32, out_f32> stays within 1e-3 of 1.
+"""
+
+import numpy as np
+import pytest
+
+from synth import Workload, make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def decode_all_modes(ctx):
+    import torch
+    import int8_kv_decode_gb300 as K
+    wl = Workload(name=f"depth{ctx}", B=2, M=1, Hq=32, Hkv=4, ctx=ctx, outliers=False, index=7)
+    x = make_workload(wl, device="cuda")
+    k8 = torch.empty((wl.Hkv, x.cap_rows, wl.d), dtype=torch.int8, device="cuda")
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((wl.Hkv, x.cap_rows), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    K.quantize_kv(x.k_rows, k8, ks)
+    K.quantize_kv(x.v_rows, v8, vs)
+    q = torch.as_tensor(x.q, device="cuda") * 5.0          # wider logits
+    rs = torch.from_numpy(x.row_start).cuda()
+    c = torch.from_numpy(x.ctx).cuda()
+    return {pm: K.decode(q, k8, ks, v8, vs, rs, c, ctx, p_mode=pm).double().cpu().numpy()
+            .reshape(-1, 128) for pm in range(5)}
+
+
+def test_fp8_p_error_does_not_grow_with_context_under_span_rounding():
+    short, long_ = decode_all_modes(2560), decode_all_modes(32768)
+    for pm in (2, 3, 4):                                   # e4m3, x448, x256
+        errs = []
+        for outs in (short, long_):
+            ref, o = outs[0], outs[pm]
+            errs.append(np.linalg.norm(o - ref) / np.linalg.norm(ref))
+            beta = float((o * ref).sum() / (ref * ref).sum())
+            assert abs(1.0 - beta) <= 1e-3, (pm, beta)   # no mass lost toward zero
+        assert errs[1] <= 1.2 * errs[0], (pm, errs)
+        assert errs[0] <= 2e-2, (pm, errs)                # e4m3's 3-bit mantissa level
