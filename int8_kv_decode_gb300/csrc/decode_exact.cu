@@ -10,9 +10,9 @@
 //
 // Only the l and o chains are inherently serial.  The scores, the running
 // max (a prefix max, which is exact in any order) and every exp are computed
-// in parallel per chunk of 128 keys; then thread i walks channel i's chain
-// through the chunk, reading the chunk's V rows from shared memory.  One CTA
-// of 128 threads per query row.
+// in parallel per chunk of 128 keys by one group of threads, while a second
+// group walks the previous chunk's chains (thread i: channel i), reading the
+// chunk's V rows from shared memory.
 #include "device_common.cuh"
 
 namespace kattn {
@@ -59,28 +59,68 @@ __device__ __forceinline__ float round_p_exact(float p, int mode) {
   }
 }
 
+// ------------------------------------------------------------ sync helpers
+constexpr uint32_t kExactSpin = 1u << 22;         // bounded waits (then the row is NaN)
+
+__device__ __forceinline__ void ex_mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void ex_mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool ex_mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kExactSpin; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+// Barrier among the 128 threads of one group (ids 1 and 2; 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int id) {
+  asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory");
+}
+
 // Shared memory of one row's CTA.  A chunk's K and V rows are staged by
-// cp.async one chunk ahead (two stages), so the serial scan reads V from
-// shared memory; the 16-byte pieces of a K row are placed at piece c ^ (key & 7)
-// so that the per-key dot products read without bank conflicts.
+// cp.async one chunk ahead (three stages); the 16-byte pieces of a K row sit at
+// piece c ^ (key & 7) so that the per-key dot products read without bank
+// conflicts.  tok holds, per key of a stage: round_p(p), v_scale, alpha, p.
+constexpr int kStages = 3;                        // K/V stages: the chains may be a chunk behind
+
 struct ExactSmem {
-  int8_t k[2][kChunk][kD];
-  int8_t v[2][kChunk][kD];
-  float4 tok[kChunk];                             // per key: round_p(p), v_scale, alpha, p
+  int8_t k[kStages][kChunk][kD];
+  int8_t v[kStages][kChunk][kD];
+  float4 tok[2][kChunk];
   ExpfConsts c;
-  int row[2][kChunk];                             // plane rows of the stage's keys
+  uint64_t full[2];                               // chunk c's tok (and V) are ready: full[c & 1]
+  uint64_t empty[2];                              // the chains are done with chunk c: empty[c & 1]
+  int row[kStages][kChunk];                       // plane rows of the stage's keys
   uint32_t q8[kD / 4];
   float red[kChunk / 32];
   float carry;
+  int ok_p, ok_c;                                 // group-wide outcome of a bounded wait
 };
 
-__global__ void __launch_bounds__(kChunk)
+// One CTA of 256 threads per query row, in two groups that overlap chunks:
+//   producers (threads 128..255, one per key of a chunk): stage chunk c + 1,
+//     then chunk c's scores, prefix max and exps -> tok[c & 1];
+//   chains (threads 0..127, one per channel): walk chunk c's o and l chains
+//     while the producers work on chunk c + 1.
+// A stage is handed over through full / empty mbarriers; one thread of each
+// group waits (bounded) and the group learns the outcome at a group barrier.
+__global__ void __launch_bounds__(2 * kChunk)
 decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   extern __shared__ __align__(16) unsigned char exact_smem[];
   ExactSmem& sm = *reinterpret_cast<ExactSmem*>(exact_smem);
 
   const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
+  const bool producer = tid >= kChunk;
+  const int gt = producer ? tid - kChunk : tid;   // key (producers) or channel (chains)
+  const int lane = gt & 31, gwarp = gt >> 5;
   const int h = blockIdx.x % p.Hq;
   const int j = (blockIdx.x / p.Hq) % p.M;
   const int b = blockIdx.x / (p.Hq * p.M);
@@ -89,14 +129,24 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   float* orow = p.out + qrow * kD;
 
   if (!sequence_valid(p, b)) {
-    orow[tid] = __int_as_float(0x7fc00000);
+    if (!producer) orow[gt] = __int_as_float(0x7fc00000);
     return;
   }
   const int L = p.ctx_len[b] + j;
   const int rs = sequence_row0(p, b);
+  const int nchunks = (L + kChunk - 1) / kChunk;
 
-  for (int i = tid; i < (int)(sizeof(ExpfConsts) / sizeof(double)); i += kChunk)
+  for (int i = tid; i < (int)(sizeof(ExpfConsts) / sizeof(double)); i += 2 * kChunk)
     reinterpret_cast<double*>(&sm.c)[i] = reinterpret_cast<const double*>(&consts)[i];
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      ex_mbar_init(&sm.full[s], 1);
+      ex_mbar_init(&sm.empty[s], 1);
+    }
+    sm.carry = -INFINITY;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
 
   // Key t is row `row` of head kh's plane: rs + t, or from the block table.
   const int64_t plane = (int64_t)kh * p.cap_rows;
@@ -105,109 +155,133 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   const float* ksb = p.k_scale + plane;
   const float* vsb = p.v_scale + plane;
 
-  // The plane rows of the chunk at t0 (thread = key) and their scales.
-  float ks_next = 0.0f, vs_next = 0.0f;
-  auto stage_rows = [&](int t0, int st) {
-    const int t = t0 + tid;
-    int row = -1;
-    if (t < L) {
-      row = p.block_table == nullptr ? rs + t : paged_row(p, b, t);
-      ks_next = ksb[row];
-      vs_next = vsb[row];
-    }
-    sm.row[st][tid] = row;
-  };
-  // The copies of that chunk's K and V rows (after a barrier publishes the
-  // rows): 128 rows x 8 pieces of 16 bytes each, 8 pieces per thread.
-  auto issue = [&](int t0, int st) {
-    const int n = min(kChunk, L - t0);
-#pragma unroll
-    for (int i = 0; i < kD / 16; ++i) {
-      const int idx = i * kChunk + tid;
-      const int u = idx >> 3, c16 = idx & 7;
-      if (u < n) {
-        const int64_t off = (int64_t)sm.row[st][u] * kD + c16 * 16;
-        cp_async16(&sm.k[st][u][(c16 ^ (u & 7)) * 16], kbase + off, 16);
-        cp_async16(&sm.v[st][u][c16 * 16], vbase + off, 16);
+  if (producer) {
+    // ---------------------------------------------------------- producers
+    float ks_next = 0.0f, vs_next = 0.0f;
+    auto stage_rows = [&](int t0, int st) {
+      const int t = t0 + gt;
+      int row = -1;
+      if (t < L) {
+        row = p.block_table == nullptr ? rs + t : paged_row(p, b, t);
+        ks_next = ksb[row];
+        vs_next = vsb[row];
       }
+      sm.row[st][gt] = row;
+    };
+    auto issue = [&](int t0, int st) {            // after a group barrier publishes the rows
+      const int n = min(kChunk, L - t0);
+#pragma unroll
+      for (int i = 0; i < kD / 16; ++i) {
+        const int idx = i * kChunk + gt;
+        const int u = idx >> 3, c16 = idx & 7;
+        if (u < n) {
+          const int64_t off = (int64_t)sm.row[st][u] * kD + c16 * 16;
+          cp_async16(&sm.k[st][u][(c16 ^ (u & 7)) * 16], kbase + off, 16);
+          cp_async16(&sm.v[st][u][c16 * 16], vbase + off, 16);
+        }
+      }
+      cp_async_commit();
+    };
+    stage_rows(0, 0);
+    group_sync(1);
+    issue(0, 0);
+
+    // int8 query: absmax over the 128 channels, then one IEEE division each.
+    const float x = p.q[qrow * kD + gt];
+    float amax = warp_max(fabsf(x));
+    if (lane == 0) sm.red[gwarp] = amax;
+    group_sync(1);
+    amax = fmaxf(fmaxf(sm.red[0], sm.red[1]), fmaxf(sm.red[2], sm.red[3]));
+    const float qs = quant_scale(amax);
+    reinterpret_cast<int8_t*>(sm.q8)[gt] = (int8_t)quant_one(x, qs);
+    group_sync(1);                                // q8 complete; red free again
+
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % kStages, tb = c & 1, t0 = c * kChunk, t = t0 + gt;
+      const bool live = t < L;
+      const int n = min(kChunk, L - t0);
+      const float ks_cur = ks_next, vs_cur = vs_next;
+      // The chains must be done with chunk c - 2: its K/V stage takes chunk
+      // c + 1 now, and its tok buffer takes chunk c.
+      if (c >= 2) {
+        if (gt == 0) sm.ok_p = ex_mbar_wait(&sm.empty[tb], ((c - 2) >> 1) & 1);
+        group_sync(1);
+        if (!sm.ok_p) break;
+      }
+      if (c + 1 < nchunks) {
+        stage_rows(t0 + kChunk, (c + 1) % kStages);
+        group_sync(1);
+        issue(t0 + kChunk, (c + 1) % kStages);
+      } else {
+        cp_async_commit();                        // an empty group keeps the count
+      }
+      cp_async_wait<1>();                         // this chunk's copies (own) landed
+      group_sync(1);                              // ... and the whole group's
+
+      float s = -INFINITY;
+      if (live) {
+        const int4* krow = reinterpret_cast<const int4*>(sm.k[st][gt]);
+        int acc = 0;
+#pragma unroll
+        for (int cc = 0; cc < kD / 16; ++cc) {
+          const int4 kv = krow[cc ^ (gt & 7)];
+          acc = __dp4a((int)kv.x, (int)sm.q8[4 * cc + 0], acc);
+          acc = __dp4a((int)kv.y, (int)sm.q8[4 * cc + 1], acc);
+          acc = __dp4a((int)kv.z, (int)sm.q8[4 * cc + 2], acc);
+          acc = __dp4a((int)kv.w, (int)sm.q8[4 * cc + 3], acc);
+        }
+        s = __fmul_rn(__fmul_rn((float)acc, __fmul_rn(qs, ks_cur)), p.sm_scale);
+      }
+      // Inclusive prefix max over the chunk, seeded with the running max.
+      float pm = s;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o2 = __shfl_up_sync(0xffffffffu, pm, off);
+        if (lane >= off) pm = fmaxf(pm, o2);
+      }
+      if (lane == 31) sm.red[gwarp] = pm;
+      const float carry = sm.carry;
+      group_sync(1);
+      for (int w = 0; w < gwarp; ++w) pm = fmaxf(pm, sm.red[w]);
+      pm = fmaxf(pm, carry);
+      // Running max before this key: the previous lane's inclusive max, or for
+      // a warp's first lane the max of the carry and all earlier warps.
+      float prev = __shfl_up_sync(0xffffffffu, pm, 1);
+      if (lane == 0) {
+        float pw = carry;
+        for (int w = 0; w < gwarp; ++w) pw = fmaxf(pw, sm.red[w]);
+        prev = pw;
+      }
+      if (live) {
+        // expf_tang(0) is exactly 1: skip the double-precision steps when the
+        // running max did not move.
+        const float a = prev == pm ? 1.0f : expf_tang(__fsub_rn(prev, pm), sm.c);
+        const float pp = s == pm ? 1.0f : expf_tang(__fsub_rn(s, pm), sm.c);
+        sm.tok[tb][gt] = make_float4(round_p_exact(pp, p.p_mode), vs_cur, a, pp);
+      }
+      group_sync(1);                              // tok complete; red and carry reads done
+      if (gt == n - 1) sm.carry = pm;
+      if (gt == 0) ex_mbar_arrive(&sm.full[tb]);
     }
-    cp_async_commit();
-  };
+    cp_async_wait<0>();
+    return;
+  }
 
-  stage_rows(0, 0);
-  __syncthreads();
-  issue(0, 0);
-
-  // int8 query: absmax over the 128 channels, then one IEEE division each.
-  const float x = p.q[qrow * kD + tid];
-  float amax = warp_max(fabsf(x));
-  if (lane == 0) sm.red[warp] = amax;
-  __syncthreads();
-  amax = fmaxf(fmaxf(sm.red[0], sm.red[1]), fmaxf(sm.red[2], sm.red[3]));
-  const float qs = quant_scale(amax);
-  reinterpret_cast<int8_t*>(sm.q8)[tid] = (int8_t)quant_one(x, qs);
-  if (tid == 0) sm.carry = -INFINITY;
-  __syncthreads();
-
+  // ---------------------------------------------------------------- chains
   float o = 0.0f, l = 0.0f;
-  for (int t0 = 0, st = 0; t0 < L; t0 += kChunk, st ^= 1) {
-    const int t = t0 + tid;
-    const bool live = t < L;
-    const int n = min(kChunk, L - t0);
-    const float ks_cur = ks_next, vs_cur = vs_next;
-    // next chunk's rows and copies, in flight during this chunk
-    if (t0 + kChunk < L) stage_rows(t0 + kChunk, st ^ 1);
-    __syncthreads();
-    if (t0 + kChunk < L) issue(t0 + kChunk, st ^ 1);
-    else cp_async_commit();                       // an empty group keeps the count
-    cp_async_wait<1>();                           // this chunk's copies (own) landed
-    __syncthreads();                              // ... and everyone's
-
-    float s = -INFINITY;
-    if (live) {
-      const int4* krow = reinterpret_cast<const int4*>(sm.k[st][tid]);
-      int acc = 0;
-#pragma unroll
-      for (int cc = 0; cc < kD / 16; ++cc) {
-        const int4 kv = krow[cc ^ (tid & 7)];
-        acc = __dp4a((int)kv.x, (int)sm.q8[4 * cc + 0], acc);
-        acc = __dp4a((int)kv.y, (int)sm.q8[4 * cc + 1], acc);
-        acc = __dp4a((int)kv.z, (int)sm.q8[4 * cc + 2], acc);
-        acc = __dp4a((int)kv.w, (int)sm.q8[4 * cc + 3], acc);
-      }
-      s = __fmul_rn(__fmul_rn((float)acc, __fmul_rn(qs, ks_cur)), p.sm_scale);
+  bool ok = true;
+  for (int c = 0; c < nchunks; ++c) {
+    const int st = c % kStages, tb = c & 1, n = min(kChunk, L - c * kChunk);
+    if (gt == 0) sm.ok_c = ex_mbar_wait(&sm.full[tb], (c >> 1) & 1);
+    group_sync(2);
+    if (!sm.ok_c) {
+      ok = false;
+      break;
     }
-    // Inclusive prefix max over the chunk, seeded with the running max.
-    float pm = s;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float o2 = __shfl_up_sync(0xffffffffu, pm, off);
-      if (lane >= off) pm = fmaxf(pm, o2);
-    }
-    if (lane == 31) sm.red[warp] = pm;
-    const float carry = sm.carry;
-    __syncthreads();
-    for (int w = 0; w < warp; ++w) pm = fmaxf(pm, sm.red[w]);
-    pm = fmaxf(pm, carry);
-    // Running max before this key: the previous lane's inclusive max, or for
-    // a warp's first lane the max of the carry and all earlier warps.
-    float prev = __shfl_up_sync(0xffffffffu, pm, 1);
-    if (lane == 0) {
-      float pw = carry;
-      for (int w = 0; w < warp; ++w) pw = fmaxf(pw, sm.red[w]);
-      prev = pw;
-    }
-    if (live) {
-      const float a = expf_tang(__fsub_rn(prev, pm), sm.c);
-      const float pp = expf_tang(__fsub_rn(s, pm), sm.c);
-      sm.tok[tid] = make_float4(round_p_exact(pp, p.p_mode), vs_cur, a, pp);
-    }
-    __syncthreads();
-    if (tid == n - 1) sm.carry = pm;
     // 32 keys at a time: first every key's term round_p(p) * (f32(v8) * vs)
     // (independent of one another), then the two chains, key by key.
-    const uint8_t* vcol = reinterpret_cast<const uint8_t*>(&sm.v[st][0][tid]);
-    const float2* tk2 = reinterpret_cast<const float2*>(sm.tok);
+    const uint8_t* vcol = reinterpret_cast<const uint8_t*>(&sm.v[st][0][gt]);
+    const float2* tk2 = reinterpret_cast<const float2*>(sm.tok[tb]);
     for (int u0 = 0; u0 < n; u0 += kSub) {
       float term[kSub];
 #pragma unroll
@@ -233,9 +307,10 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
         }
       }
     }
-    __syncthreads();
+    group_sync(2);                                // every chain is done with chunk c
+    if (gt == 0) ex_mbar_arrive(&sm.empty[tb]);
   }
-  orow[tid] = __fdiv_rn(o, l);
+  orow[gt] = ok ? __fdiv_rn(o, l) : __int_as_float(0x7fc00000);
 }
 
 }  // namespace
@@ -247,7 +322,7 @@ cudaError_t launch_decode_exact(const DecodeParams& p, const ExpfConsts& c,
   cudaError_t e = cudaFuncSetAttribute(decode_exact_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_exact_kernel<<<(unsigned)rows, kChunk, smem, stream>>>(p, c);
+  decode_exact_kernel<<<(unsigned)rows, 2 * kChunk, smem, stream>>>(p, c);
   return cudaGetLastError();
 }
 
