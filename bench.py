@@ -38,7 +38,8 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES_NOMINAL = 129 * 1024 * 1024
 HEAD_DIM = 128
-KERNEL_SOURCES = ["decode_fast.cu", "decode_split.cuh", "device_common.cuh", "kattn_internal.cuh"]
+KERNEL_SOURCES = ["decode_fast.cu", "decode_split.cuh", "decode_tc.cu", "device_common.cuh",
+                  "kattn_internal.cuh"]
 
 
 # ------------------------------------------------------------ accounting --
@@ -70,6 +71,14 @@ def load_peak_hbm():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def roofline_kernel(g: int, M: int, exact: bool) -> str:
+    """The decode kernel a call launches: exact mode, P.V on tcgen05 for
+    17..32 query rows per (sequence, kv head), else the mma.sync split pass."""
+    if exact:
+        return "decode_exact_kernel"
+    return "decode_tc_kernel" if 16 < g * M <= 32 else "decode_fast_kernel"
 
 
 def kernel_source_sha() -> str:
@@ -533,7 +542,7 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
                      "traffic": profiled_traffic(wl.name, sha),
-                     "kernel": "decode_exact_kernel" if exact else "decode_fast_kernel",
+                     "kernel": roofline_kernel(wl.Hq // wl.Hkv, wl.M, exact),
                      "algorithmic_bytes_per_launch": algo,
                      "avg_launch_us": decode_s * 1e6, "kernel_source_sha": sha},
         "kv_frac_of_step": (kvb / (elapsed / args.steps) / 1e9) / peak,

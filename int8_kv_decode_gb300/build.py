@@ -32,6 +32,7 @@ SOURCES = {
     "qk_debug.cu": [],
     "decode_fast.cu": [],
     "decode_fast_paged.cu": [],
+    "decode_tc.cu": [],
     "decode_noalloc.cu": [],
     "decode_exact.cu": ["--fmad=false"],
     "expf_constants.cu": ["--fmad=false"],

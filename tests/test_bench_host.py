@@ -92,3 +92,13 @@ def test_all_cores_oracle_baseline_runs_in_spawned_processes():
     from synth import WORKLOADS
     gbs, cores, secs = bench.time_oracle_all_cores(WORKLOADS["tiny"], 0.2)
     assert cores >= 1 and secs >= 0.2 and gbs > 0
+
+
+def test_roofline_kernel_follows_the_dispatch():
+    # 17..32 query rows per (sequence, kv head) run the tcgen05 P.V kernel.
+    assert bench.roofline_kernel(8, 1, False) == "decode_fast_kernel"
+    assert bench.roofline_kernel(8, 2, False) == "decode_fast_kernel"      # R = 16
+    assert bench.roofline_kernel(8, 3, False) == "decode_tc_kernel"        # R = 24
+    assert bench.roofline_kernel(8, 4, False) == "decode_tc_kernel"        # R = 32
+    assert bench.roofline_kernel(8, 5, False) == "decode_fast_kernel"      # R = 40
+    assert bench.roofline_kernel(8, 4, True) == "decode_exact_kernel"
