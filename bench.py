@@ -89,6 +89,19 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def traffic_key(workload: str, page_rows: int = 0) -> str:
+    """The name a workload's traffic line carries: the paged layout is its own."""
+    return f"{workload}_paged{page_rows}" if page_rows else workload
+
+
+def paged_rows(block_table, page_rows: int, seqs, keys):
+    """Physical cache row of key keys[i] of sequence seqs[i] in a paged layout."""
+    import numpy as np
+    seqs = np.asarray(seqs, np.int64)
+    keys = np.asarray(keys, np.int64)
+    return block_table[seqs, keys // page_rows].astype(np.int64) * page_rows + keys % page_rows
+
+
 def profiled_traffic(workload: str, sha: str):
     """DRAM bytes per launch of the decode kernel from a committed ncu summary
     line 'traffic_per_launch <workload> <source sha> <bytes>', if the kernel
@@ -317,11 +330,13 @@ def run_reference(args):
     return 0
 
 
-def workload_config(wl, ctx, note=None, l2=None, launch=None, p_mode="f32", exact=False):
+def workload_config(wl, ctx, note=None, l2=None, launch=None, p_mode="f32", exact=False,
+                    page_rows=0):
     import numpy as np
     c = {"workload": wl.name, "B": wl.B, "M": wl.M, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
          "ctx": wl.ctx if isinstance(wl.ctx, int) else f"{wl.ctx[0]}[{wl.ctx[1]},{wl.ctx[2]}]",
-         "mean_ctx": float(np.mean(ctx)), "p_mode": p_mode, "exact_mode": bool(exact)}
+         "mean_ctx": float(np.mean(ctx)), "p_mode": p_mode, "exact_mode": bool(exact),
+         "layout": f"paged, {page_rows}-row pages in shuffled order" if page_rows else "contiguous"}
     if l2:
         c["l2"] = l2
     if launch:
@@ -371,6 +386,20 @@ def run_ours(args):
     dst = torch.tensor(append_rows(x.row_start, x.ctx, M), dtype=torch.int64, device=dev)
     knew = x.k_rows[dst].contiguous()
     vnew = x.v_rows[dst].contiguous()
+    P = int(args.page_rows)
+    bt = None
+    if P:
+        # The same rows in a paged layout (shuffled pages): every cache copy is
+        # re-laid out and the contiguous copy dropped; the step's appends go to
+        # the paged rows of keys ctx - 1 .. ctx + M - 2.
+        import numpy as np
+        from synth.paging import page_layout, paged_copy
+        L = page_layout(x.ctx, x.row_start, M, P, seed=rank)
+        caches = [paged_copy(L, *cc, seed=c) for c, cc in enumerate(caches)]
+        bt = torch.from_numpy(L.block_table).to(dev)
+        seqs = np.repeat(np.arange(B), M)
+        keys = np.concatenate([np.arange(int(c) - 1, int(c) - 1 + M) for c in x.ctx])
+        dst = torch.from_numpy(paged_rows(L.block_table, P, seqs, keys)).to(dev)
     x.k_rows = x.v_rows = None                          # free the float32 prefill rows
     torch.cuda.empty_cache()
     q = x.q.contiguous()
@@ -386,13 +415,18 @@ def run_ours(args):
 
     def decode(i):
         k8, ks, v8, vs = caches[i % n_copies]
+        if P:
+            K.decode_paged(q, k8, ks, v8, vs, bt, P, ctx, max_ctx, out=out,
+                           workspace=None if exact else ws, p_mode=pm, exact_mode=exact)
+            return
         K.decode(q, k8, ks, v8, vs, rs, ctx, max_ctx, out=out, workspace=None if exact else ws,
                  p_mode=pm, exact_mode=exact)
 
     def step(i):
         k8, ks, v8, vs = caches[i % n_copies]
-        if exact:
-            # exact mode has no fused append: the two appends, then the decode
+        if exact or P:
+            # exact mode and the paged layout have no fused append: the two
+            # appends, then the decode
             K.quantize_kv_rows(knew, dst, k8, ks)
             K.quantize_kv_rows(vnew, dst, v8, vs)
             decode(i)
@@ -537,11 +571,11 @@ def run_ours(args):
             wl, x.ctx, l2=(f"inputs larger than L2: {kvb / 1e9:.2f} GB KV per step x "
                            f"{n_copies} rotating cache copies vs {l2 / 2**20:.0f} MiB L2"),
             launch="eager" if args.no_graphs else "one CUDA graph replay per step",
-            p_mode=args.p_mode, exact=exact),
+            p_mode=args.p_mode, exact=exact, page_rows=P),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
-                     "traffic": profiled_traffic(wl.name, sha),
+                     "traffic": profiled_traffic(traffic_key(wl.name, P), sha),
                      "kernel": roofline_kernel(wl.Hq // wl.Hkv, wl.M, exact),
                      "algorithmic_bytes_per_launch": algo,
                      "avg_launch_us": decode_s * 1e6, "kernel_source_sha": sha},
@@ -549,7 +583,8 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": total_bytes / e_tmax / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": (3 if exact else K.decode_launch_count(B, M, Hq, Hkv, max_ctx)) * args.steps,
+        "gpu_launches": ((2 if exact or P else 0) +
+                         (1 if exact else K.decode_launch_count(B, M, Hq, Hkv, max_ctx))) * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -575,6 +610,9 @@ def main(argv=None):
                     help="rounding of the P that multiplies V")
     ap.add_argument("--exact", action="store_true",
                     help="time exact mode (token-order scan, table-driven exp) instead of fast mode")
+    ap.add_argument("--page-rows", type=int, default=0,
+                    help="time the paged layout: pages of this many rows (32 * 2^k) in shuffled "
+                         "order (default: the contiguous cache)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every step eagerly instead of replaying CUDA graphs")
     ap.add_argument("--ref-sequences", type=int, default=2,

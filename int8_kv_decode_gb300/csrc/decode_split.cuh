@@ -998,7 +998,7 @@ cudaError_t launch_modes(const DecodeParams& p, const TmaMaps& maps, cudaStream_
 cudaError_t launch_split_paged(const DecodeParams& p, const TmaMaps& maps, cudaStream_t stream);
 
 // The split-KV pass for 17..32 query rows per (sequence, kv head) with P.V on
-// the fifth-generation tensor cores (decode_tc.cu), contiguous cache.
+// the fifth-generation tensor cores (decode_tc.cu), contiguous or paged cache.
 cudaError_t launch_split_tc(const DecodeParams& p, const TmaMaps& maps, cudaStream_t stream);
 
 }  // namespace kattn

@@ -47,6 +47,7 @@ struct __align__(1024) TcSmem {
   uint64_t qbar, mbar;                           // queries landed / MMAs done
   __align__(16) float alpha[kTcRows];            // this block's alpha per row
   float wm[kSpansPerCta][kTcRows], wl[kSpansPerCta][kTcRows], wd[kSpansPerCta][kTcRows];
+  int brow[2][kSplitC / kBlockBk];               // paged: cache rows of an item's blocks, by parity
   uint32_t tmem;
   // A copy or an MMA group never completed, by block parity: a warp may flag
   // block n + 1 before a slower one has read the flag of block n.
@@ -142,15 +143,22 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
-// Cache row (2-D view) of block k of the item: the spans' blocks in order.
-__device__ __forceinline__ int tc_block_row(const Item& it, int k, const int (&nbs)[kSpansPerCta],
-                                            int M) {
-  int s = 0;
-  while (s < kSpansPerCta - 1 && k >= nbs[s]) k -= nbs[s++];
-  return span_of(it, s, M).row + k * kBlockBk;
+// Paged layout: the block-table entry of key `key` of sequence b, and the
+// cache row it gives (paged_row in two steps, so that the table load can be
+// issued an item ahead of its use).  An entry outside the pool flags
+// KATTN_DEVERR_BAD_PAGE and reads page 0.
+__device__ __forceinline__ int tc_page_entry(const DecodeParams& p, int b, int key) {
+  return __ldg(p.block_table + (int64_t)b * p.max_pages + (key >> p.page_shift));
+}
+__device__ __forceinline__ int tc_page_row(const DecodeParams& p, int page, int key) {
+  if ((unsigned)page >= (unsigned)p.n_pages) {
+    if (p.err_word) atomicOr(p.err_word, KATTN_DEVERR_BAD_PAGE);
+    page = 0;
+  }
+  return (page << p.page_shift) | (key & ((1 << p.page_shift) - 1));
 }
 
-template <int PM>
+template <int PM, bool PG>
 __global__ void __launch_bounds__(kTcWarps * 32, kTcCtasPerSm)
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   extern __shared__ unsigned char smem_raw[];
@@ -211,6 +219,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     bulk_load(sm.qbuf, p.qpack + ((size_t)x.b * p.Hkv + x.kh) * kQBytes, kQBytes, &sm.qbar);
     q_pending = true;
   };
+  // Block k of an item holds keys w * kSplitC + 32k .. + 31 (every span but
+  // the last non-empty one is full).  Paged: the rows come from brow, filled
+  // by warp 0 -- the current item's (par) before the item starts, the next
+  // item's (par ^ 1) after the current item's first block (nrows).
+  int par = 0;
+  bool nrows = !PG;                               // thread 0: brow[par ^ 1] is filled
   // Thread 0: issue the copies of blocks [issued, limit) -- this item's, then
   // the next item's.  A block's stage was last read by the block kTcStages
   // earlier, which every warp has passed (a CTA barrier follows each block).
@@ -218,9 +232,13 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     while (issued < limit) {
       const int k = issued - gbase;
       int row;
-      if (k < nbt) row = tc_block_row(it, k, nbs, M);
-      else if (k - nbt < nbt_n) row = tc_block_row(nxt, k - nbt, nbs_n, M);
-      else break;
+      if (k < nbt) {
+        row = PG ? sm.brow[par][k] : it.row + it.w * kSplitC + k * kBlockBk;
+      } else if (k - nbt < nbt_n && nrows) {
+        row = PG ? sm.brow[par ^ 1][k - nbt] : nxt.row + nxt.w * kSplitC + (k - nbt) * kBlockBk;
+      } else {
+        break;
+      }
       const int st = issued % kTcStages;
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       mbar_expect_tx(&sm.full[st], 2 * kBlockBytes);
@@ -231,12 +249,26 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   };
   if (tid == 0 && it.b >= 0) fetch_queries(it);
   float ksn[4], vsn[4];                           // the next span's k and v scales
-  load_span_scales<false>(p, it, span_of(it, 0, M), lane, ksn, vsn);
+  load_span_scales<PG>(p, it, span_of(it, 0, M), lane, ksn, vsn);
 
   for (int t = blockIdx.x; t < total && !failed; t += G) {
     const int ctx = it.ctx, b = it.b, kh = it.kh;
     nbt = blocks_of(it, nbs);
     nbt_n = blocks_of(nxt, nbs_n);
+    int pentry = 0;                               // paged, warp 0 lane k: the next item's block k
+    if constexpr (PG) {
+      if (warp == 0) {
+        if (t == (int)blockIdx.x) {               // the first item: its rows now
+          if (lane < nbt) {
+            const int key = it.w * kSplitC + lane * kBlockBk;
+            sm.brow[par][lane] = it.row + tc_page_row(p, tc_page_entry(p, it.b, key), key);
+          }
+          __syncwarp();
+        }
+        if (lane < nbt_n) pentry = tc_page_entry(p, nxt.b, nxt.w * kSplitC + lane * kBlockBk);
+      }
+      nrows = false;
+    }
     if (tid == 0) produce(gbase + kTcStages);
     // every span's accumulator starts at +0 (each warp its own lanes)
     {
@@ -280,8 +312,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
         vsp[e] = vsn[e];
       }
       // the next span's scales, one span ahead (this item's, else the next item's first)
-      if (s + 1 < kSpansPerCta) load_span_scales<false>(p, it, span_of(it, s + 1, M), lane, ksn, vsn);
-      else load_span_scales<false>(p, nxt, span_of(nxt, 0, M), lane, ksn, vsn);
+      if (s + 1 < kSpansPerCta) load_span_scales<PG>(p, it, span_of(it, s + 1, M), lane, ksn, vsn);
+      else load_span_scales<PG>(p, nxt, span_of(nxt, 0, M), lane, ksn, vsn);
       // 2^E per row from the largest v_scale among the keys the row sees
       float up_row[2], down_row[2];
       {
@@ -503,6 +535,14 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
           tc_fence_before();
           __syncthreads();
         }
+        if (PG && kb == 0 && warp == 0) {        // the next item's block rows
+          if (lane < nbt_n) {
+            const int key = nxt.w * kSplitC + lane * kBlockBk;
+            sm.brow[par ^ 1][lane] = nxt.row + tc_page_row(p, pentry, key);
+          }
+          __syncwarp();
+          nrows = true;
+        }
         if (tid == 0) {
           tc_fence_after();
           const uint32_t dcol = tmem + 32 * s;
@@ -594,6 +634,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     gbase += nbt;
     it = nxt;
     nxt = load_item(p, t + 2 * G, total);
+    par ^= 1;
   }
 
   // ---- leave: every copy and MMA in flight lands (bounded) before the
@@ -612,11 +653,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTcCols));
 }
 
-template <int PM>
+template <int PM, bool PG>
 cudaError_t launch_tc_mode(const DecodeParams& p, const TmaMaps& maps, cudaStream_t stream) {
   const int smem = (int)sizeof(TcSmem) + 1024;   // + alignment slack
   constexpr int kThreads = kTcWarps * 32;
-  const auto kern = decode_tc_kernel<PM>;
+  const auto kern = decode_tc_kernel<PM, PG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   static std::atomic<int> slots_cache[kMaxDevices];
@@ -644,18 +685,24 @@ cudaError_t launch_tc_mode(const DecodeParams& p, const TmaMaps& maps, cudaStrea
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, stream, p, maps);
 }
 
+template <bool PG>
+cudaError_t launch_tc_layout(const DecodeParams& p, const TmaMaps& maps, cudaStream_t stream) {
+  switch (p.p_mode) {
+    case KATTN_P_BF16: return launch_tc_mode<KATTN_P_BF16, PG>(p, maps, stream);
+    case KATTN_P_E4M3: return launch_tc_mode<KATTN_P_E4M3, PG>(p, maps, stream);
+    case KATTN_P_E4M3_X448: return launch_tc_mode<KATTN_P_E4M3_X448, PG>(p, maps, stream);
+    case KATTN_P_E4M3_X256: return launch_tc_mode<KATTN_P_E4M3_X256, PG>(p, maps, stream);
+    default: return launch_tc_mode<KATTN_P_F32, PG>(p, maps, stream);
+  }
+}
+
 }  // namespace
 
 // The split-KV pass on the fifth-generation tensor cores for 17..32 query rows
-// per (sequence, kv head), contiguous cache.
+// per (sequence, kv head), contiguous or paged cache.
 cudaError_t launch_split_tc(const DecodeParams& p, const TmaMaps& maps, cudaStream_t stream) {
-  switch (p.p_mode) {
-    case KATTN_P_BF16: return launch_tc_mode<KATTN_P_BF16>(p, maps, stream);
-    case KATTN_P_E4M3: return launch_tc_mode<KATTN_P_E4M3>(p, maps, stream);
-    case KATTN_P_E4M3_X448: return launch_tc_mode<KATTN_P_E4M3_X448>(p, maps, stream);
-    case KATTN_P_E4M3_X256: return launch_tc_mode<KATTN_P_E4M3_X256>(p, maps, stream);
-    default: return launch_tc_mode<KATTN_P_F32>(p, maps, stream);
-  }
+  return p.block_table != nullptr ? launch_tc_layout<true>(p, maps, stream)
+                                  : launch_tc_layout<false>(p, maps, stream);
 }
 
 }  // namespace kattn

@@ -102,3 +102,13 @@ def test_roofline_kernel_follows_the_dispatch():
     assert bench.roofline_kernel(8, 4, False) == "decode_tc_kernel"        # R = 32
     assert bench.roofline_kernel(8, 5, False) == "decode_fast_kernel"      # R = 40
     assert bench.roofline_kernel(8, 4, True) == "decode_exact_kernel"
+
+
+def test_paged_rows_and_traffic_key():
+    # Key t of sequence b lives at block_table[b][t // P] * P + t % P; the
+    # paged layout's traffic line carries its own name.
+    bt = np.array([[3, 1, -1], [0, 2, 4]], np.int32)
+    got = bench.paged_rows(bt, 32, [0, 0, 1, 1], [0, 33, 64, 5])
+    assert got.tolist() == [96, 33, 128, 5]
+    assert bench.traffic_key("serving_b256_m4", 64) == "serving_b256_m4_paged64"
+    assert bench.traffic_key("serving_b256_m4") == "serving_b256_m4"
