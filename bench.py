@@ -38,8 +38,14 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES_NOMINAL = 129 * 1024 * 1024
 HEAD_DIM = 128
-KERNEL_SOURCES = ["decode_fast.cu", "decode_split.cuh", "decode_tc.cu", "device_common.cuh",
-                  "kattn_internal.cuh"]
+# The source files each decode kernel is built from: a traffic line stays
+# valid while they are unchanged.
+_COMMON_SOURCES = ["device_common.cuh", "kattn_internal.cuh"]
+KERNEL_SOURCES = {
+    "decode_fast_kernel": ["decode_fast.cu", "decode_split.cuh"] + _COMMON_SOURCES,
+    "decode_tc_kernel": ["decode_fast.cu", "decode_split.cuh", "decode_tc.cu"] + _COMMON_SOURCES,
+    "decode_exact_kernel": ["decode_exact.cu"] + _COMMON_SOURCES,
+}
 
 
 # ------------------------------------------------------------ accounting --
@@ -81,9 +87,9 @@ def roofline_kernel(g: int, M: int, exact: bool) -> str:
     return "decode_tc_kernel" if 16 < g * M <= 32 else "decode_fast_kernel"
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(kernel: str = "decode_fast_kernel", paged: bool = False) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel] + (["decode_fast_paged.cu"] if paged else []):
         with open(os.path.join(ROOT, "int8_kv_decode_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -538,7 +544,8 @@ def run_ours(args):
     peak, peak_kind = load_peak_hbm()
     algo = kvb + qob
     achieved = algo / decode_s / 1e9
-    sha = kernel_source_sha()
+    rkernel = roofline_kernel(wl.Hq // wl.Hkv, wl.M, exact)
+    sha = kernel_source_sha(rkernel, paged=bool(P) and not exact)
     clocks = None
     try:
         with open(clock_path) as f:
@@ -576,7 +583,7 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
                      "traffic": profiled_traffic(traffic_key(wl.name, P), sha),
-                     "kernel": roofline_kernel(wl.Hq // wl.Hkv, wl.M, exact),
+                     "kernel": rkernel,
                      "algorithmic_bytes_per_launch": algo,
                      "avg_launch_us": decode_s * 1e6, "kernel_source_sha": sha},
         "kv_frac_of_step": (kvb / (elapsed / args.steps) / 1e9) / peak,
