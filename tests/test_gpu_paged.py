@@ -96,10 +96,11 @@ def test_paged_full_size_serving_m4_equals_contiguous():
     assert K.get_device_status(ws) == 0
 
 
-def test_paged_bad_tables_are_flagged_without_touching_other_sequences():
+@pytest.mark.parametrize("M,Hq", [(2, 8), (4, 16)])    # R = 8 (mma.sync) and R = 32 (tcgen05)
+def test_paged_bad_tables_are_flagged_without_touching_other_sequences(M, Hq):
     import torch
     import int8_kv_decode_gb300 as K
-    wl = custom("paged_bad", 6, 2, 8, 2, ("uniform", 100, 900), outliers=False)
+    wl = custom(f"paged_bad_m{M}", 6, M, Hq, 2, ("uniform", 100, 900), outliers=False)
     c = upload(wl)
     pc = Paged(c, 64, seed=3)
     ws = K.alloc_workspace(wl.B, wl.M, wl.Hq, c.x.max_ctx)
