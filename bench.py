@@ -613,7 +613,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-all-cores", action="store_true",
                     help="skip the all-cores oracle baseline (the single-threaded one stays)")
     ap.add_argument("--p-mode", default="f32", choices=["f32", "bf16", "e4m3", "e4m3x448",
-                                                        "e4m3x256"],
+                                                        "e4m3x256", "e4m3direct"],
                     help="rounding of the P that multiplies V")
     ap.add_argument("--exact", action="store_true",
                     help="time exact mode (token-order scan, table-driven exp) instead of fast mode")

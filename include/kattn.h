@@ -63,7 +63,13 @@ enum kattn_p_mode {
   KATTN_P_BF16 = 1,     /* round to bfloat16, nearest-even */
   KATTN_P_E4M3 = 2,     /* round to fp8 e4m3 (OCP), nearest-even, saturating */
   KATTN_P_E4M3_X448 = 3, /* e4m3(p * 448) / 448 */
-  KATTN_P_E4M3_X256 = 4  /* e4m3(p * 256) / 256 (both scalings exact in float32) */
+  KATTN_P_E4M3_X256 = 4, /* e4m3(p * 256) / 256 (both scalings exact in float32) */
+  /* e4m3 P fed straight to the tensor-core P.V (the same page's closing
+   * question; fast mode only).  p~ = e4m3(p); the P.V operand of key t is the
+   * float32 product p~ * v_scale_t rounded once to 11 significant bits
+   * (f16 precision, nearest-even), and V enters exact as f16.  That drops the
+   * low-part MMA the other modes use to carry p~ * v_scale at 22 bits. */
+  KATTN_P_E4M3_DIRECT = 5
 };
 
 #define KATTN_HEAD_DIM 128 /* the only supported head_dim */
@@ -158,7 +164,8 @@ int kattn_quantize_kv_rows(const float* x, int n_rows, int n_kv, int d,
  *            NaN outputs only); no memory outside the arrays is touched.
  * max_ctx:   host-side upper bound on ctx_len (sizes the grid).
  * sm_scale:  0 selects RN_f32(1/sqrt(d)).
- * p_mode:    a kattn_p_mode.
+ * p_mode:    a kattn_p_mode (KATTN_P_E4M3_DIRECT with exact_mode = 1 ->
+ *            KATTN_ERR_INVALID_ARG: the exact scan has no tensor-core operand).
  * exact_mode = 0 (fast): split-KV over spans of C keys, merged in a fixed
  *   order; float32 accumulation; deterministic run to run, and the bytes of
  *   out[b][j][h] depend only on that row's own keys, so column j equals an

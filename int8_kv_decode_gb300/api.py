@@ -13,7 +13,7 @@ import torch
 
 from . import _lib
 
-P_MODES = {"f32": 0, "bf16": 1, "e4m3": 2, "e4m3x448": 3, "e4m3x256": 4}
+P_MODES = {"f32": 0, "bf16": 1, "e4m3": 2, "e4m3x448": 3, "e4m3x256": 4, "e4m3direct": 5}
 
 
 def _stream(device) -> int:

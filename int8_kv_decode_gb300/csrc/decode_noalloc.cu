@@ -46,7 +46,7 @@ int check_args(const float* q, const int8_t* k, const float* k_scale, const int8
   if (M > KATTN_MAX_M || (Hq / Hkv) * M > KATTN_MAX_ROWS) return KATTN_ERR_UNSUPPORTED;
   if ((int64_t)max_ctx + M - 1 > (int64_t)INT32_MAX / 2) return KATTN_ERR_INVALID_ARG;
   if ((int64_t)Hkv * cap_rows > (int64_t)INT32_MAX - 4096) return KATTN_ERR_UNSUPPORTED;
-  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_DIRECT) return KATTN_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
   if (B == 0) return KATTN_OK;
   if (kattn::workspace_layout(B, M, Hq, max_ctx).total > kScratchBytes)

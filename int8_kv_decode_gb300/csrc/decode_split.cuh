@@ -235,7 +235,7 @@ template <int PM>
 __device__ __forceinline__ float round_p_t(float p) {
   if constexpr (PM == KATTN_P_BF16) {
     return bf16_round(p);
-  } else if constexpr (PM == KATTN_P_E4M3) {
+  } else if constexpr (PM == KATTN_P_E4M3 || PM == KATTN_P_E4M3_DIRECT) {
     return e4m3_round(p);
   } else if constexpr (PM == KATTN_P_E4M3_X256) {
     return __fmul_rn(e4m3_round(__fmul_rn(p, 256.0f)), 1.0f / 256.0f);   // both exact
@@ -759,7 +759,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 #pragma unroll
           for (int nr = 0; nr < NR; ++nr) {
             mma_f16(o[md][nr], af, bhi[nr]);
-            mma_f16(o[md][nr], af, blo[nr]);
+            if constexpr (PM != KATTN_P_E4M3_DIRECT) mma_f16(o[md][nr], af, blo[nr]);
           }
         }
       }
@@ -987,6 +987,8 @@ cudaError_t launch_modes(const DecodeParams& p, const TmaMaps& maps, cudaStream_
     case KATTN_P_E4M3: return launch_variant<NR, NG, KATTN_P_E4M3, PG>(p, maps, stream);
     case KATTN_P_E4M3_X448: return launch_variant<NR, NG, KATTN_P_E4M3_X448, PG>(p, maps, stream);
     case KATTN_P_E4M3_X256: return launch_variant<NR, NG, KATTN_P_E4M3_X256, PG>(p, maps, stream);
+    case KATTN_P_E4M3_DIRECT:
+      return launch_variant<NR, NG, KATTN_P_E4M3_DIRECT, PG>(p, maps, stream);
     default: return launch_variant<NR, NG, KATTN_P_F32, PG>(p, maps, stream);
   }
 }

@@ -493,8 +493,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
           for (int hf = 0; hf < 2; ++hf) {
             *reinterpret_cast<uint32_t*>(sm.pb[hf][0] + op_off(r, 2 * c)) = ph[hf][0];
             *reinterpret_cast<uint32_t*>(sm.pb[hf][0] + op_off(r, 2 * c + 8)) = ph[hf][1];
-            *reinterpret_cast<uint32_t*>(sm.pb[hf][1] + op_off(r, 2 * c)) = pl[hf][0];
-            *reinterpret_cast<uint32_t*>(sm.pb[hf][1] + op_off(r, 2 * c + 8)) = pl[hf][1];
+            if constexpr (PM != KATTN_P_E4M3_DIRECT) {   // that mode has no low part
+              *reinterpret_cast<uint32_t*>(sm.pb[hf][1] + op_off(r, 2 * c)) = pl[hf][0];
+              *reinterpret_cast<uint32_t*>(sm.pb[hf][1] + op_off(r, 2 * c + 8)) = pl[hf][1];
+            }
           }
           uint8_t* vdst = sm.vt[warp >> 1];
 #pragma unroll
@@ -549,7 +551,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             tc_mma(dcol, smem_desc(sm.vt[hf]), smem_desc(sm.pb[hf][0]));
-            tc_mma(dcol, smem_desc(sm.vt[hf]), smem_desc(sm.pb[hf][1]));
+            if constexpr (PM != KATTN_P_E4M3_DIRECT)
+              tc_mma(dcol, smem_desc(sm.vt[hf]), smem_desc(sm.pb[hf][1]));
           }
           tc_commit(&sm.mbar);
           if (kb == 0 && nxt.b >= 0) fetch_queries(nxt);   // every warp has read this item's
@@ -692,6 +695,7 @@ cudaError_t launch_tc_layout(const DecodeParams& p, const TmaMaps& maps, cudaStr
     case KATTN_P_E4M3: return launch_tc_mode<KATTN_P_E4M3, PG>(p, maps, stream);
     case KATTN_P_E4M3_X448: return launch_tc_mode<KATTN_P_E4M3_X448, PG>(p, maps, stream);
     case KATTN_P_E4M3_X256: return launch_tc_mode<KATTN_P_E4M3_X256, PG>(p, maps, stream);
+    case KATTN_P_E4M3_DIRECT: return launch_tc_mode<KATTN_P_E4M3_DIRECT, PG>(p, maps, stream);
     default: return launch_tc_mode<KATTN_P_F32, PG>(p, maps, stream);
   }
 }

@@ -77,8 +77,9 @@ void set_workspace(DecodeParams& p, const WorkspaceLayout& w, void* workspace);
 int run_decode(DecodeParams& p, int p_mode, int exact_mode, float sm_scale, const int8_t* v,
                const float* v_scale, float* out, void* workspace, size_t workspace_bytes,
                void* stream) {
-  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_DIRECT) return KATTN_ERR_INVALID_ARG;
   if (exact_mode != 0 && exact_mode != 1) return KATTN_ERR_INVALID_ARG;
+  if (exact_mode && p_mode == KATTN_P_E4M3_DIRECT) return KATTN_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
   if (p.B == 0) return KATTN_OK;
   if (!v || !v_scale || !out) return KATTN_ERR_INVALID_ARG;
@@ -223,7 +224,7 @@ int kattn_decode_append(const float* q, const float* k_new, const float* v_new,
                         void* workspace, size_t workspace_bytes, void* stream) {
   int st = check_common(q, k, k_scale, row_start, 8, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
   if (st != KATTN_OK) return st;
-  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_DIRECT) return KATTN_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
   if (n_new < 0 || row_stride_elems < (int64_t)Hkv * d) return KATTN_ERR_INVALID_ARG;
   if (n_new > 0 && (!k_new || !v_new || !dst_rows)) return KATTN_ERR_INVALID_ARG;
@@ -306,7 +307,7 @@ int kattn_decode_shard(const float* q, const int8_t* k, const float* k_scale, co
   // key positions of the shard are int32 on the device
   if (((int64_t)shard + 1) * win_per_shard * kSplitC > (int64_t)INT32_MAX / 2)
     return KATTN_ERR_INVALID_ARG;
-  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_X256) return KATTN_ERR_INVALID_ARG;
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_DIRECT) return KATTN_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
   if (B == 0) return KATTN_OK;
   if (!v || !v_scale || !partials) return KATTN_ERR_INVALID_ARG;

@@ -19,14 +19,17 @@ Three ways to evaluate 6:
 
 * ``reference`` with p_mode 0 -- the plain definition in float64:
       out = sum_t exp(s_t - max s) vdeq_t / sum_t exp(s_t - max s)
-* ``reference`` with p_mode 1..3 -- the blockwise online softmax of
+* ``reference`` with p_mode 1..5 -- the blockwise online softmax of
   "在 agent 时代如何快速验证 kernel 对精度的影响" (section "注意力权重"), with
   the rounding points placed where a split-KV kernel places them: keys are
   cut into splits of C keys (absolute positions [sC, (s+1)C)), each split
   into blocks of Bk keys; per block the running max m is updated first,
   p = f32(exp(s - m)) is rounded once to float32, the row sum uses p and the
   PV product uses round_p(p).  Splits are then merged in split order with
-  weights exp(m_s - max_s m_s).  All other arithmetic is float64.
+  weights exp(m_s - max_s m_s).  All other arithmetic is float64.  Mode 5
+  multiplies the int8 V values by pv_operand(round_p(p), vs): the float32
+  product p~ * vs rounded to 11 significant bits (rounding.py); mode 5 has
+  no ``exact`` form.
 * ``exact`` -- a float32 emulation of the sequential scan: one token at a
   time in token order, every float32 operation rounded on its own (no fused
   multiply-add), exp by the table-driven expf_tang:
@@ -51,7 +54,7 @@ import numpy as np
 
 from .expf_tang import expf_tang
 from .quant import quantize_queries
-from .rounding import round_p, round_p_f32
+from .rounding import DIRECT, pv_operand, round_p, round_p_f32
 
 
 def default_sm_scale(d: int) -> np.float32:
@@ -90,8 +93,11 @@ def row_softmax_f64(s, vdeq) -> np.ndarray:
     return (p @ vdeq) / p.sum()
 
 
-def row_online_mirrored(s, vdeq, p_mode: int, C: int, Bk: int) -> np.ndarray:
-    """Blockwise online softmax with round_p, splits of C and blocks of Bk."""
+def row_online_mirrored(s, vdeq, p_mode: int, C: int, Bk: int, v8=None, vs=None) -> np.ndarray:
+    """Blockwise online softmax with round_p, splits of C and blocks of Bk.
+
+    vdeq [L][d] float64 = vs * v8; mode 5 (DIRECT) needs v8 [L][d] and vs [L]
+    instead, since its PV operand is p~ * vs rounded."""
     s = np.asarray(s, np.float32)
     L = s.shape[0]
     parts = []
@@ -104,7 +110,11 @@ def row_online_mirrored(s, vdeq, p_mode: int, C: int, Bk: int) -> np.ndarray:
             alpha = math.exp(m - m_new) if m != -math.inf else 0.0
             p = np.exp(sb - m_new).astype(np.float32)        # one f32 rounding
             l = l * alpha + float(p.astype(np.float64).sum())
-            o = o * alpha + round_p(p, p_mode) @ vdeq[b0:b1]
+            if p_mode == DIRECT:
+                o = o * alpha + pv_operand(round_p(p, p_mode), vs[b0:b1], p_mode) @ \
+                    np.asarray(v8[b0:b1], np.float64)
+            else:
+                o = o * alpha + round_p(p, p_mode) @ vdeq[b0:b1]
             m = m_new
         parts.append((m, l, o))
     m_all = max(pm for pm, _, _ in parts)
@@ -225,5 +235,6 @@ def decode(q, k8, ks, v8, vs, row_start, ctx, *, sm_scale=None, p_mode=0,
                     if p_mode == 0:
                         out[b, j, h] = row_softmax_f64(s[i], vdeq)
                     else:
-                        out[b, j, h] = row_online_mirrored(s[i], vdeq, p_mode, C, Bk)
+                        out[b, j, h] = row_online_mirrored(s[i], vdeq, p_mode, C, Bk,
+                                                           v8=vr, vs=vs[kh, r0:r0 + L])
     return out

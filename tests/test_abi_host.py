@@ -96,7 +96,9 @@ def test_decode_validation(lib):
     assert _decode(lib, q=0x1008) == MISAL
     assert _decode(lib, k=0x1004) == MISAL
     assert _decode(lib, rs=0x1004) == MISAL
-    assert _decode(lib, p_mode=5) == INVALID
+    assert _decode(lib, p_mode=6) == INVALID
+    assert _decode(lib, p_mode=-1) == INVALID
+    assert _decode(lib, p_mode=5, exact=1) == INVALID     # e4m3 direct: fast mode only
     assert _decode(lib, exact=2) == INVALID
     assert _decode(lib, sm=float("nan")) == INVALID
     assert _decode(lib, max_ctx=0) == INVALID
@@ -130,7 +132,8 @@ def test_decode_paged_validation(lib):
     assert _decode_paged(lib, page=96, cap=288) == UNSUP   # not a power of two
     assert _decode_paged(lib, page=64, cap=224) == INVALID  # pages do not tile the planes
     assert _decode_paged(lib, d=64) == UNSUP
-    assert _decode_paged(lib, p_mode=5) == INVALID
+    assert _decode_paged(lib, p_mode=6) == INVALID
+    assert _decode_paged(lib, p_mode=5, exact=1) == INVALID
     assert _decode_paged(lib, ws=0) == WS
     assert _decode_paged(lib, B=0) == 0
 
@@ -187,7 +190,7 @@ def test_shard_validation(lib):
     assert _decode_shard(lib, part=0) == INVALID
     assert _decode_shard(lib, part=0x1008) == MISAL
     assert _decode_shard(lib, d=64) == UNSUP
-    assert _decode_shard(lib, p_mode=5) == INVALID
+    assert _decode_shard(lib, p_mode=6) == INVALID
     assert _decode_shard(lib, ws=0) == WS
     assert _decode_shard(lib, B=0) == 0
     assert _merge_shards(lib, n=0) == INVALID

@@ -44,12 +44,12 @@ def decode_all_modes(ctx):
     rs = torch.from_numpy(x.row_start).cuda()
     c = torch.from_numpy(x.ctx).cuda()
     return {pm: K.decode(q, k8, ks, v8, vs, rs, c, ctx, p_mode=pm).double().cpu().numpy()
-            .reshape(-1, 128) for pm in range(5)}
+            .reshape(-1, 128) for pm in range(6)}
 
 
 def test_fp8_p_error_does_not_grow_with_context_under_span_rounding():
     short, long_ = decode_all_modes(2560), decode_all_modes(32768)
-    for pm in (2, 3, 4):                                   # e4m3, x448, x256
+    for pm in (2, 3, 4, 5):                                # e4m3, x448, x256, direct
         errs = []
         for outs in (short, long_):
             ref, o = outs[0], outs[pm]

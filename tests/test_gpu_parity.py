@@ -112,7 +112,7 @@ def test_fast_f32_spec_verify_sampled():
     assert_f32_tolerance(got, ref, row_mask(got.shape, rows))
 
 
-@pytest.mark.parametrize("p_mode", [1, 2, 3, 4])
+@pytest.mark.parametrize("p_mode", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("name", ["tiny", "qwen_layer"])
 def test_fast_rounded_p_modes(name, p_mode):
     import int8_kv_decode_gb300 as K
@@ -447,3 +447,25 @@ def test_long_rows_alone_equal_the_batch(p_mode):
     rows = sample_rows(c.x, 24, seed=5)
     if p_mode == 0:
         assert_f32_tolerance(full, oracle_decode(c, rows=rows), row_mask(full.shape, rows))
+
+
+def test_e4m3_direct_mode_columns_and_oracle():
+    # p_mode 5 (e4m3 P into the tensor-core P.V, one f16 operand): the M = 4
+    # batch (32 rows per kv head: the tcgen05 kernel) against the oracle with
+    # the same rounding, every draft column equal to the M = 1 decode (the
+    # mma.sync kernel) byte for byte, and no exact-mode form.
+    import int8_kv_decode_gb300 as K
+    C, Bk = K.get_tiling()
+    wl = custom("direct_m4", 5, 4, 16, 2, ("uniform", 300, 2500), outliers=True, index=77)
+    c = upload(wl)
+    got = run(c, p_mode=5).cpu().numpy()
+    rows = sample_rows(c.x, 16, seed=5)
+    same = oracle_decode(c, p_mode=5, C=C, Bk=Bk, rows=rows)
+    m = row_mask(got.shape, rows)
+    assert rel_l2(got[m], same[m]) <= ROUNDED_REL_L2
+    for j in range(wl.M):
+        one = K.decode(c.q[:, j:j + 1].contiguous(), c.k8, c.ks, c.v8, c.vs, c.rs, c.ctx + j,
+                       c.x.max_ctx + j, p_mode=5).cpu().numpy()
+        assert np.array_equal(bits(got[:, j:j + 1]), bits(one)), j
+    with pytest.raises(Exception):
+        run(c, p_mode=5, exact_mode=True)

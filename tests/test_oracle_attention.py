@@ -266,3 +266,46 @@ def test_exact_mode_is_sequential_float32():
     o = [f(f(o[i] * a) + f(p * vd1[i])) for i in range(2)]
     expect = np.array([f(o[0] / l), f(o[1] / l)], np.float32)
     assert np.array_equal(A.rows_exact_f32(s, v8, vs, 0)[0], expect)
+
+
+# ---- mode 5: e4m3 P into the tensor-core P.V, operand p~ * vs rounded to the
+# f16 significand.
+
+def test_direct_mode_single_key_returns_the_rounded_scale_times_v8():
+    # One key: p = 1, p~ = 1, the operand is f16_significand(vs), l = 1.
+    rng = np.random.default_rng(60)
+    q, k8, ks, v8, vs, rs, ctx = tiny_case(rng, B=1, M=1, ctx=(1,))
+    out = A.decode(q, k8, ks, v8, vs, rs, ctx, p_mode=R.DIRECT)
+    g = q.shape[2] // k8.shape[0]
+    for h in range(q.shape[2]):
+        r = rs[0]
+        expect = R.f16_significand(np.float32(vs[h // g, r])) * v8[h // g, r].astype(np.float64)
+        assert np.array_equal(out[0, 0, h], expect)
+
+
+def test_direct_mode_equals_e4m3_when_every_scale_is_a_power_of_two():
+    # e4m3 values have at most 4 significant bits, so p~ * 2^k is exact in 11
+    # bits and mode 5 computes what mode 2 computes, bit for bit.
+    rng = np.random.default_rng(61)
+    q, k8, ks, v8, vs, rs, ctx = tiny_case(rng, B=2, M=2, ctx=(150, 70), d=16)
+    vs = np.ldexp(1.0, rng.integers(-9, -2, vs.shape)).astype(np.float32)
+    a = A.decode(q, k8, ks, v8, vs, rs, ctx, p_mode=R.DIRECT, C=64, Bk=16)
+    b = A.decode(q, k8, ks, v8, vs, rs, ctx, p_mode=2, C=64, Bk=16)
+    assert np.array_equal(a, b)
+
+
+def test_direct_mode_stays_within_the_f16_rounding_of_e4m3():
+    # Each PV term moves by at most 2^-11 relative, the row sum not at all.
+    rng = np.random.default_rng(62)
+    q, k8, ks, v8, vs, rs, ctx = tiny_case(rng, B=2, M=2, ctx=(300, 120), d=16, scale=2.0)
+    a = A.decode(q, k8, ks, v8, vs, rs, ctx, p_mode=R.DIRECT, C=64, Bk=16)
+    b = A.decode(q, k8, ks, v8, vs, rs, ctx, p_mode=2, C=64, Bk=16)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert 0.0 < rel <= 2.0 ** -11
+
+
+def test_direct_mode_has_no_exact_scan():
+    rng = np.random.default_rng(63)
+    q, k8, ks, v8, vs, rs, ctx = tiny_case(rng, B=1, M=1, ctx=(4,))
+    with pytest.raises(ValueError):
+        A.decode(q, k8, ks, v8, vs, rs, ctx, p_mode=R.DIRECT, mode="exact")

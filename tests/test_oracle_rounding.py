@@ -4,6 +4,7 @@ section "注意力权重")."""
 import itertools
 
 import numpy as np
+import pytest
 import torch
 
 from conftest import read_golden
@@ -137,3 +138,50 @@ def test_x256_brute_force_against_the_e4m3_value_set():
     out = R.round_p(mids.astype(np.float32), 4)
     assert np.array_equal(out, grid[2:])
     assert np.array_equal(R.round_p_f32(grid.astype(np.float32), 4).astype(np.float64), grid)
+
+
+# ---- mode 5: e4m3 P straight into the tensor-core P.V ("注意力权重", closing
+# question).  Its operand p~ * v_scale is rounded to the f16 significand.
+
+def test_f16_significand_matches_numpy_float16_in_its_normal_range():
+    # numpy's float32 -> float16 cast rounds to nearest-even: in f16's normal
+    # range it is the same 11-significant-bit rounding.
+    rng = np.random.default_rng(50)
+    v = np.ldexp(rng.uniform(1.0, 2.0, 20000), rng.integers(-14, 15, 20000)).astype(np.float32)
+    ties = np.float32(1.0) + np.float32(2.0 ** -11) * np.arange(1, 64, 2, dtype=np.float32)
+    v = np.concatenate([v, ties])
+    want = v.astype(np.float16).astype(np.float64)
+    assert np.array_equal(R.f16_significand(v), want)
+
+
+def test_f16_significand_has_no_exponent_floor():
+    # Below f16's normal range the kernel scales by a power of two first, so
+    # the rounding keeps 11 significant bits: equal to the float16 cast of the
+    # value moved into the normal range and moved back.
+    rng = np.random.default_rng(51)
+    v = np.ldexp(rng.uniform(1.0, 2.0, 5000), rng.integers(-60, -15, 5000)).astype(np.float32)
+    e = np.frexp(v.astype(np.float64))[1]
+    k = 1 - e                                    # v * 2^k in [1, 2)
+    want = np.ldexp(np.ldexp(v.astype(np.float64), k).astype(np.float16).astype(np.float64), -k)
+    assert np.array_equal(R.f16_significand(v), want)
+    assert np.all(np.abs(R.f16_significand(v) / v - 1.0) <= 2.0 ** -11)
+
+
+def test_pv_operand_rounds_only_in_the_direct_mode():
+    rng = np.random.default_rng(52)
+    p = R.e4m3(rng.uniform(0.0, 1.0, 4000).astype(np.float32)).astype(np.float32)
+    vs = rng.uniform(0.001, 0.9, 4000).astype(np.float32)
+    prod32 = np.multiply(p, vs, dtype=np.float32)
+    assert np.array_equal(R.pv_operand(p, vs, R.DIRECT), R.f16_significand(prod32))
+    for mode in (0, 1, 2, 3, 4):
+        assert np.array_equal(R.pv_operand(p, vs, mode), p.astype(np.float64) * vs.astype(np.float64))
+    # a product that 11 bits hold exactly is unchanged: e4m3 values (<= 4
+    # significant bits) times powers of two
+    pw = np.ldexp(1.0, rng.integers(-8, 3, 4000)).astype(np.float32)
+    assert np.array_equal(R.pv_operand(p, pw, R.DIRECT), p.astype(np.float64) * pw)
+    assert np.array_equal(R.round_p(p, R.DIRECT), R.round_p(p, 2))
+
+
+def test_direct_mode_has_no_exact_form():
+    with pytest.raises(ValueError):
+        R.round_p_f32(np.ones(3, np.float32), R.DIRECT)
