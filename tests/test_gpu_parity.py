@@ -190,7 +190,7 @@ def test_batch_size_invariance():
 
 
 @pytest.mark.parametrize("g,M", [(1, 1), (4, 1), (8, 1), (1, 8), (4, 3), (8, 2), (4, 5), (8, 3),
-                                 (8, 4), (8, 5), (8, 8)])
+                                 (8, 4), (8, 5), (8, 8), (3, 8), (16, 2), (32, 1)])
 def test_shape_sweep(g, M):
     # ctx around the block and split sizes ("海光 DCU 实测" §4: one shape being
     # exact proves nothing about the others).
