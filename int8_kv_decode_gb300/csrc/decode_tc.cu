@@ -12,16 +12,19 @@
 // the M = 1 kernel's bytes and batch invariance holds.
 //
 // Layout: one CTA of 4 warps per work item (sequence, 512-key window, kv
-// head), persistent over the work list.  The window's 16 blocks of 32 keys
-// go through in order, span after span; for each block warp w computes the
-// scores and P of rows 8w..8w+7 and converts a quarter of V to f16 (d =
-// channels of its m-tiles).  One thread issues the block's four MMAs:
+// head), persistent over the work list, 4 CTAs per SM (tensor memory: 128
+// columns each).  The window's 16 blocks of 32 keys go through in order, span
+// after span; for each block warp w computes the scores and P of rows
+// 8w..8w+7 and converts keys 8w..8w+7 of V to f16 for all 128 channels.  One
+// thread issues the block's four MMAs (two with p_mode e4m3-direct, which has
+// no low part):
 //   D_s[d][row] += Vt[d][key] * P[row][key]   (M = 128 channels, N = 32
 // rows, K = 16 keys), D_s = span s's accumulator in tensor memory (lanes =
 // channels, columns 32s .. 32s + 31 = rows).  When a row's running max moves,
 // the four warps rescale their 32 lanes of D_s by alpha before the MMAs.  At
 // the window's end each warp merges the four spans for its 32 channels in the
-// same order as the M = 1 kernel.
+// same order as the M = 1 kernel.  PG: the paged cache, block rows from the
+// block table.
 #include "decode_split.cuh"
 
 namespace kattn {
@@ -37,9 +40,9 @@ constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcRows >> 3) << 17) | ((1
 
 struct __align__(1024) TcSmem {
   uint8_t ring[kTcStages][2][kBlockBytes];       // K and V blocks of 32 keys (128-byte swizzle)
-  // MMA operands of the block in flight, no swizzle, K-major, 16 keys per
-  // half: element (row, key) at (row / 8) * 256 + (key / 8) * 128 + (row % 8)
-  // * 16 + (key % 8) * 2.
+  // MMA operands of the block in flight (no swizzle, K-major, 16 keys per
+  // half): element (row, key) at (row / 8) * 256 + (key / 8) * 128 +
+  // (row % 8) * 16 + (key % 8) * 2.
   uint8_t vt[2][128 * 16 * 2];                   // [half] V transposed: rows = channels
   uint8_t pb[2][2][kTcRows * 16 * 2];            // [half][hi | lo] P: rows = query rows
   uint8_t qbuf[kTcRows * (kD + 4)];              // the item's int8 rows, then scales
@@ -123,7 +126,7 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
-// 32 consecutive columns of the calling warp's 32 lanes (waits).
+// Store 32 consecutive columns of the calling warp's 32 lanes (waits for the store).
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
