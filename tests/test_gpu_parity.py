@@ -228,15 +228,15 @@ def test_odd_row_count_over_several_windows(g, M):
         assert np.array_equal(bits(got[:, j:j + 1]), bits(one))
 
 
-@pytest.mark.parametrize("B", [1000, 2100])
-def test_many_short_sequences(B):
+@pytest.mark.parametrize("B,M,Hq", [(1000, 1, 8), (2100, 1, 8), (2100, 4, 16)])
+def test_many_short_sequences(B, M, Hq):
     # Many short sequences: most work items are one short window, so warps
     # of a CTA reach the next item at very different times.  Above 2048
     # sequences the work list is written by its own kernel rather than by
     # the query-packing launch.  Sampled rows against the oracle, and the
     # bytes of each half of the batch decoded alone.
     import int8_kv_decode_gb300 as K
-    wl = custom(f"many{B}", B, 1, 8, 2, ("uniform", 1, 1200), outliers=False)
+    wl = custom(f"many{B}_m{M}", B, M, Hq, 2, ("uniform", 1, 1200), outliers=False)
     c = upload(wl)
     got = run(c).cpu().numpy()
     rows = sample_rows(c.x, 40, seed=3)
@@ -247,12 +247,14 @@ def test_many_short_sequences(B):
         assert np.array_equal(bits(got[lo:hi]), bits(half)), (lo, hi)
 
 
-def test_decode_replays_in_a_cuda_graph():
+@pytest.mark.parametrize("shape", ["spec_verify", "r32"])   # mma.sync (R = 40), tcgen05 (R = 32)
+def test_decode_replays_in_a_cuda_graph(shape):
     # The three launches of a fast decode, captured once and replayed, give
     # the bytes of an ordinary call.
     import torch
     import int8_kv_decode_gb300 as K
-    c = upload(WORKLOADS["spec_verify"])
+    c = upload(WORKLOADS["spec_verify"] if shape == "spec_verify" else
+               custom("graph_r32", 12, 4, 16, 2, ("uniform", 100, 3000), outliers=True))
     B, M, Hq, _ = c.q.shape
     ws = K.alloc_workspace(B, M, Hq, c.x.max_ctx)
     ref = run(c, workspace=ws).cpu().numpy()
