@@ -91,6 +91,19 @@ def test_spec_verify_shards_equal_single_gpu_bytes(n_shards, p_mode):
     assert K.get_device_status(mws) == 0
 
 
+@pytest.mark.parametrize("n_shards", [2, 3])
+def test_r32_shards_equal_single_gpu_bytes(n_shards):
+    # 32 query rows per kv head (M = 4, GQA 8): the tcgen05 kernel's window
+    # partials in shard mode, gathered and merged, give the single-GPU bytes.
+    import int8_kv_decode_gb300 as K
+    wl = custom("cp_r32", 8, 4, 16, 2, ("uniform", 300, 5000), outliers=True)
+    c = upload(wl)
+    ref = run(c).cpu().numpy()
+    out, mws = cp_decode(c, n_shards, seed=70 + n_shards)
+    assert np.array_equal(bits(out.cpu().numpy()), bits(ref))
+    assert K.get_device_status(mws) == 0
+
+
 def test_short_and_single_window_sequences():
     # sequences of 1 key, one window, exactly one window, and long ones; with
     # 4 shards most sequences have no key in the last shards

@@ -364,14 +364,17 @@ def test_full_size_serving_sampled():
     assert_f32_tolerance(np.array(got), np.array(ref))
 
 
-@pytest.mark.parametrize("name,p_mode", [("spec_verify", 0), ("spec_verify", 2), ("qwen_layer", 0)])
+@pytest.mark.parametrize("name,p_mode", [("spec_verify", 0), ("spec_verify", 2), ("qwen_layer", 0),
+                                         ("r32", 0)])
 def test_decode_append_equals_separate_calls(name, p_mode):
     # kattn_decode_append: the M draft rows of every sequence quantized into
     # the cache inside the decode launch -- the same cache bytes and outputs
     # as kattn_quantize_kv_rows twice followed by kattn_decode.
     import torch
     import int8_kv_decode_gb300 as K
-    wl = WORKLOADS[name]
+    # r32: 32 query rows per kv head (M = 4, GQA 8), the tcgen05 kernel
+    wl = WORKLOADS[name] if name != "r32" else custom("append_r32", 6, 4, 16, 2,
+                                                       ("uniform", 200, 3000), outliers=True)
     x = make_workload(wl, rep=5)
     dev = "cuda"
     k_rows = torch.from_numpy(x.k_rows).to(dev)

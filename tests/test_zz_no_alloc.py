@@ -14,7 +14,7 @@ import ctypes
 import numpy as np
 import pytest
 
-from helpers import assert_f32_tolerance, run, upload
+from helpers import assert_f32_tolerance, custom, run, upload
 from synth import WORKLOADS
 
 
@@ -31,12 +31,14 @@ def _noalloc(c, out):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["qwen_layer", "spec_verify"])
+@pytest.mark.parametrize("name", ["qwen_layer", "spec_verify", "r32"])
 def test_noalloc_matches_the_workspace_entry_point_on_two_calls(name):
     import torch
     import __graft_entry__
     __graft_entry__.build()
-    c = upload(WORKLOADS[name])
+    # r32: 32 query rows per kv head (M = 4, GQA 8), the tcgen05 kernel
+    c = upload(WORKLOADS[name] if name != "r32" else
+               custom("noalloc_r32", 6, 4, 16, 2, ("uniform", 200, 3000), outliers=True))
     ref = run(c).cpu().numpy()                  # kattn_decode, caller-owned workspace
     for _ in range(2):
         out = torch.full_like(c.q, float("nan"))
