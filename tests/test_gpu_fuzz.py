@@ -11,8 +11,11 @@ Checks:
   ("Kestrel_VLLM - 18", §二);
 - a sub-batch decoded alone equals, byte for byte, its rows in the whole batch;
 - the device error word stays clear;
-- every third case with contexts up to 3000: exact mode equals the oracle's
-  float32 emulation, byte for byte, on sampled rows.
+- every third case with contexts up to 3000 (and a P mode with an exact form):
+  exact mode equals the oracle's float32 emulation, byte for byte, on sampled
+  rows.
+
+The P mode is drawn over all six, e4m3 fed straight to the P.V MMA included.
 
 ("海光 DCU 实测" §4: one shape being right proves nothing about the others.)
 """
@@ -55,7 +58,7 @@ def draw_case(i):
         ctx = rng.integers(1, 3000, B)                            # a few windows
     else:
         ctx = np.exp(rng.uniform(0, np.log(6000), B)).astype(np.int64) + 1   # ragged, long
-    return dict(B=B, M=M, g=g, Hkv=Hkv, ctx=ctx.astype(np.int32), p_mode=int(rng.integers(0, 5)),
+    return dict(B=B, M=M, g=g, Hkv=Hkv, ctx=ctx.astype(np.int32), p_mode=int(rng.integers(0, 6)),
                 outliers=bool(rng.integers(0, 2)), page=int(rng.choice([0, 32, 64, 128])),
                 seed=int(rng.integers(0, 1 << 30)))
 
@@ -122,8 +125,8 @@ def test_random_case(i):
               int(c.x.ctx[lo:hi].max()), d["p_mode"]).cpu().numpy()
     assert np.array_equal(bits(full[lo:hi]), bits(sub)), (lo, hi)
 
-    # 4. exact mode on sampled rows
-    if i % 3 == 0 and int(c.x.ctx.max()) <= 3000:
+    # 4. exact mode on sampled rows (p_mode 5 has no exact form)
+    if i % 3 == 0 and int(c.x.ctx.max()) <= 3000 and d["p_mode"] != 5:
         if d["page"]:
             ex = K.decode_paged(c.q, kp, ksp, vp, vsp, bt, d["page"], c.ctx, max_ctx,
                                 p_mode=d["p_mode"], exact_mode=True).cpu().numpy()
