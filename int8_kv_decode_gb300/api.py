@@ -111,6 +111,9 @@ def decode(q, k, k_scale, v, v_scale, row_start, ctx_len, max_ctx: int, *,
 
     q [B][M][Hq][d] f32; k, v [Hkv][cap][d] int8; k_scale, v_scale [Hkv][cap]
     f32; row_start [B] int64; ctx_len [B] int32 (all on the same CUDA device).
+    p_mode: an int or a name of P_MODES -- "f32", "bf16", "e4m3", "e4m3x448",
+    "e4m3x256", or "e4m3direct" (e4m3 P fed straight to the P.V MMA as one
+    f16 operand p~ * v_scale; fast mode only).
     workspace: a zeroed uint8 tensor of decode_workspace_size(...) bytes
     (fast mode); allocated here with torch if None.
     """
