@@ -474,8 +474,9 @@ def run_ours(args):
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clock_path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_rank{rank}.csv")
+    import tempfile
+    clock_fd, clock_path = tempfile.mkstemp(prefix=f"kattn_bench_clocks_rank{rank}_", suffix=".csv")
+    os.close(clock_fd)
     sampler = start_clock_sampler(gpu_id, clock_path) if rank == 0 else (None, None)
     time.sleep(0.3)                                       # sampler start-up
 
@@ -552,6 +553,11 @@ def run_ours(args):
             clocks = parse_clocks(f.read(), wall0, wall1)
     except OSError:
         pass
+    finally:
+        try:
+            os.unlink(clock_path)
+        except OSError:
+            pass
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:

@@ -301,7 +301,8 @@ int kattn_merge_shards(const float* partials, const int32_t* ctx_len, int B, int
  *     KATTN_ERR_WORKSPACE before anything is enqueued.
  *   - The first call on a device looks up the array's address on that device
  *     (with that device current); make that first call before any stream
- *     capture begins.
+ *     capture begins.  If the lookup fails the call returns KATTN_ERR_CUDA
+ *     and the next call on that device tries the lookup again.
  *   - Each call clears the array's error word on `stream` (cudaMemsetAsync)
  *     before decoding; the array keeps the rest of the last call's contents.
  *   - All calls on a device share the one array: calls that overlap on the

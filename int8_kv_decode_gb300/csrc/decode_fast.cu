@@ -330,11 +330,6 @@ bool encode_cache_map(CUtensorMap* map, const int8_t* base, int64_t rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 17..32 rows: P.V on the fifth-generation tensor cores (decode_tc.cu).
-#ifndef KATTN_SPLIT_TC
-#define KATTN_SPLIT_TC 1
-#endif
-
 // The split-KV pass over a contiguous cache, by the rows R of a CTA.  (The
 // cache layout is a template parameter, so this kernel carries none of the
 // paged lookups.)
@@ -342,11 +337,7 @@ cudaError_t launch_split_contiguous(const DecodeParams& p, const TmaMaps& maps,
                                     cudaStream_t stream) {
   if (p.R <= 8) return launch_modes<1, 1, false>(p, maps, stream);
   if (p.R <= 16) return launch_modes<2, 1, false>(p, maps, stream);
-#if KATTN_SPLIT_TC
-  if (p.R <= 32) return launch_split_tc(p, maps, stream);
-#else
-  if (p.R <= 32) return launch_modes<2, 2, false>(p, maps, stream);
-#endif
+  if (p.R <= 32) return launch_split_tc(p, maps, stream);   // P.V on tcgen05
   if (p.R <= 48) return launch_modes<3, 2, false>(p, maps, stream);
   return launch_modes<4, 2, false>(p, maps, stream);
 }

@@ -3,20 +3,12 @@
 // parallel with the contiguous variants (decode_fast.cu).
 #include "decode_split.cuh"
 
-#ifndef KATTN_SPLIT_TC
-#define KATTN_SPLIT_TC 1
-#endif
-
 namespace kattn {
 
 cudaError_t launch_split_paged(const DecodeParams& p, const TmaMaps& maps, cudaStream_t stream) {
   if (p.R <= 8) return launch_modes<1, 1, true>(p, maps, stream);
   if (p.R <= 16) return launch_modes<2, 1, true>(p, maps, stream);
-#if KATTN_SPLIT_TC
   if (p.R <= 32) return launch_split_tc(p, maps, stream);   // P.V on tcgen05 (decode_tc.cu)
-#else
-  if (p.R <= 32) return launch_modes<2, 2, true>(p, maps, stream);
-#endif
   if (p.R <= 48) return launch_modes<3, 2, true>(p, maps, stream);
   return launch_modes<4, 2, true>(p, maps, stream);
 }

@@ -24,12 +24,27 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 
+// The array's address on each device, looked up on the first call that
+// succeeds in doing so: a failed lookup stores nothing, so a later call
+// tries again (for instance once memory is no longer short).
 struct DeviceScratch {
-  std::once_flag once;
+  std::mutex lock;
   void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
 };
 DeviceScratch g_device_scratch[kMaxDevices];
+
+// The scratch address on the current device `dev`, or nullptr if the
+// lookup failed (the caller reports KATTN_ERR_CUDA).
+void* scratch_on(int dev) {
+  DeviceScratch& ds = g_device_scratch[dev];
+  std::lock_guard<std::mutex> guard(ds.lock);
+  if (ds.ptr == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess) return nullptr;
+    ds.ptr = p;
+  }
+  return ds.ptr;
+}
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
@@ -72,19 +87,18 @@ extern "C" int kattn_decode_noalloc(const float* q, const int8_t* k, const float
   if (st != KATTN_OK || B == 0) return st;
 
   // Set-up, once per device and with that device current: find where the
-  // scratch array lives on it.
+  // scratch array lives on it (retried by the next call if it failed).
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return KATTN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return KATTN_ERR_UNSUPPORTED;
-  DeviceScratch& ds = g_device_scratch[dev];
-  std::call_once(ds.once, [&ds] { ds.err = cudaGetSymbolAddress(&ds.ptr, g_scratch); });
-  if (ds.err != cudaSuccess || ds.ptr == nullptr) return KATTN_ERR_CUDA;
+  void* scratch = scratch_on(dev);
+  if (scratch == nullptr) return KATTN_ERR_CUDA;
 
   // The array keeps whatever the previous call left in it.  The header (the
   // error word) must start at zero; the work list, the quantized queries and
   // the partials are always written before they are read.
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ds.ptr, 0, 256, s) != cudaSuccess) return KATTN_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return KATTN_ERR_CUDA;
   return kattn_decode(q, k, k_scale, v, v_scale, row_start, ctx_len, B, M, Hq, Hkv, d, cap_rows,
-                      max_ctx, sm_scale, p_mode, 0, out, ds.ptr, kScratchBytes, stream);
+                      max_ctx, sm_scale, p_mode, 0, out, scratch, kScratchBytes, stream);
 }

@@ -63,10 +63,7 @@ struct TmaMaps {
 namespace {
 
 
-#ifndef KATTN_STAGES
-#define KATTN_STAGES 2
-#endif
-constexpr int kRing = KATTN_STAGES;            // TMA stages per warp
+constexpr int kRing = 2;                       // TMA stages per warp
 constexpr int kBlockBytes = kBlockBk * kD;     // one K (or V) block: 4 KB
 constexpr uint32_t kSpinLimit = 1u << 22;      // bounded mbarrier waits
 static_assert(kBlockBk == 32, "the MMA layout below takes a block as two halves of 16 keys");
@@ -74,15 +71,10 @@ static_assert(kSpanC == 4 * kBlockBk, "span scales are held as 4 registers per l
 
 
 
-// QK on the int8 MMA when a warp holds one n-tile of query rows (see the kernel).
-#ifndef KATTN_QK_INT8
-#define KATTN_QK_INT8 1
-#endif
-
 template <int NR, int NG>
 struct __align__(1024) SmemT {
   static constexpr int kRows = NG * NR * 8;                  // query rows of the CTA (rpad)
-  static constexpr int kF = (KATTN_QK_INT8 && NR == 1) ? 1 : 0;   // no f16 fragments
+  static constexpr int kF = NR == 1 ? 1 : 0;                 // int8 QK: no f16 fragments
 
   uint8_t ring[kSpansPerCta][kRing][2][kBlockBytes];         // per span: [stage][K|V]
   float slot[NG][2][NR * 8 * kD];                            // span merge, fragment order
@@ -351,7 +343,7 @@ template <int NR, int NG, int PM, bool PG>
 __global__ void __launch_bounds__(kSpansPerCta * 32 * NG, NR == 1 ? 3 : (NG == 1 ? 2 : 1))
 decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   using Smem = SmemT<NR, NG>;
-  constexpr bool kQK8 = KATTN_QK_INT8 && NR == 1;
+  constexpr bool kQK8 = NR == 1;                  // QK on the int8 MMA (one n-tile)
   constexpr int RG = NR * 8;                      // rows per warp group
   constexpr int RP = Smem::kRows;                 // rows per CTA (the packed query rows)
   constexpr int kWarps = kSpansPerCta * NG;

@@ -27,9 +27,14 @@ Modules:
   hashdump   -- FNV-1a 64 row hashes and the first differing row (§3.4's
                 parity-dump method)
 
-Parity unpinned: the absolute accuracy of the rounded-P modes against the
-infinitely precise softmax is not pinned by anything on the pages; only the
-same-rounding comparison is.
+Parity unpinned:
+  * the absolute accuracy of the rounded-P modes against the infinitely
+    precise softmax is not pinned by anything on the pages; only the
+    same-rounding comparison is;
+  * the order of the score scaling, s = ((f32(S) * (qs * ks)) * sm_scale),
+    each product rounded once to float32: the pages are silent on it, so no
+    pin outside the oracle fixes it (its tests restate it; the GPU path is
+    held to it only through the end-to-end tolerances and exact mode).
 """
 
 from . import quant, rounding, expf_tang, attention, hashdump  # noqa: F401

@@ -11,7 +11,9 @@ What is computed, per query row (sequence b, draft column j, query head h):
      must equal an M=1 decode that saw the same tokens).
   4. S_t = sum_i q8_i * k8_t,i exactly (int64 here; |S| <= 128*127^2).
   5. s_t = ((f32(S_t) * (qs * ks_t)) * sm_scale) in float32, sm_scale =
-     RN_f32(1/sqrt(d)) unless given.
+     RN_f32(1/sqrt(d)) unless given.  Parity unpinned: this order is the
+     reading used here; the pages print no scaling order ("在 agent 时代如何
+     快速验证 kernel 对精度的影响" writes only q @ K^T / sqrt(d)).
   6. softmax over t and the weighted sum of dequantized V rows
      vdeq_t = vs_t * v8_t.
 

@@ -15,6 +15,21 @@ F32_MAX_ABS = 1e-4      # fast mode, f32 P: max |delta|
 F32_REL_L2 = 1e-5       # fast mode, f32 P: relative L2
 ROUNDED_REL_L2 = 2e-3   # rounded-P modes against the oracle with the same rounding
 
+# The rounding points of the rounded-P modes: spans of C = 128 keys at fixed
+# positions, online-softmax blocks of Bk = 32 keys.  The oracle mirrors them
+# from these constants; the library must report the same tiling, so a change
+# to the kernels' tiling fails the tests instead of being followed silently.
+SPAN_C = 128
+BLOCK_BK = 32
+
+
+def pinned_tiling():
+    """(C, Bk) for the oracle's rounded-P mirror, after checking that the
+    library under test reports exactly that tiling."""
+    import int8_kv_decode_gb300 as K
+    assert K.get_tiling() == (SPAN_C, BLOCK_BK), K.get_tiling()
+    return SPAN_C, BLOCK_BK
+
 
 @dataclasses.dataclass
 class GpuCase:
@@ -100,3 +115,55 @@ def row_mask(shape, rows):
     for (b, j, h) in rows:
         m[b, j, h] = True
     return m
+
+
+def bits(a):
+    """float32 array as its uint32 bit patterns (byte-for-byte comparisons)."""
+    return np.ascontiguousarray(np.asarray(a, np.float32)).view(np.uint32)
+
+
+def device_case(name, rep=0):
+    """A full-size workload drawn on the GPU and quantized there:
+    (inputs, k8, ks, v8, vs, row_start, ctx) with the caches and the two
+    index arrays on the device."""
+    import torch
+    import int8_kv_decode_gb300 as K
+    from synth import WORKLOADS
+    wl = WORKLOADS[name]
+    x = make_workload(wl, rep=rep, device="cuda")
+    k8 = torch.empty((wl.Hkv, x.cap_rows, wl.d), dtype=torch.int8, device="cuda")
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((wl.Hkv, x.cap_rows), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    K.quantize_kv(x.k_rows, k8, ks)
+    K.quantize_kv(x.v_rows, v8, vs)
+    rs = torch.from_numpy(x.row_start).cuda()
+    ctx = torch.from_numpy(x.ctx).cuda()
+    return x, k8, ks, v8, vs, rs, ctx
+
+
+def oracle_sequence_cache(x, b, k8=None, ks=None, v8=None, vs=None):
+    """The oracle's own quantized cache of sequence b of a device-drawn
+    workload, from the generator's float32 rows (copied to the host).  When
+    the device caches are given, their bytes for the sequence must equal the
+    oracle's (quantization parity)."""
+    lo, hi = x.rows_of(b)
+    ok8, oks = oracle.quant.quantize_kv(x.k_rows[lo:hi].cpu().numpy())
+    ov8, ovs = oracle.quant.quantize_kv(x.v_rows[lo:hi].cpu().numpy())
+    if k8 is not None:
+        assert np.array_equal(k8[:, lo:hi].cpu().numpy(), ok8)
+        assert np.array_equal(bits(ks[:, lo:hi].cpu().numpy()), bits(oks))
+        assert np.array_equal(v8[:, lo:hi].cpu().numpy(), ov8)
+        assert np.array_equal(bits(vs[:, lo:hi].cpu().numpy()), bits(ovs))
+    return ok8, oks, ov8, ovs
+
+
+def oracle_sequence_rows(x, b, cache, rows, **kw):
+    """Oracle outputs of sequence b alone (its cache from oracle_sequence_cache)
+    for the (j, h) pairs in rows: an array [M][Hq][d], NaN elsewhere."""
+    q = x.q[b:b + 1]
+    q = q.cpu().numpy() if hasattr(q, "cpu") else np.asarray(q)
+    ok8, oks, ov8, ovs = cache
+    out = oracle.attention.decode(q, ok8, oks, ov8, ovs, np.array([0]), x.ctx[b:b + 1],
+                                  rows=[(0, j, h) for (j, h) in rows], **kw)
+    return out[0]

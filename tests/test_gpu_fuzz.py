@@ -23,8 +23,8 @@ The P mode is drawn over all six, e4m3 fed straight to the P.V MMA included.
 import numpy as np
 import pytest
 
-from helpers import (ROUNDED_REL_L2, assert_f32_tolerance, custom, oracle_decode, rel_l2,
-                     row_mask, sample_rows, upload)
+from helpers import (ROUNDED_REL_L2, assert_f32_tolerance, custom, oracle_decode,
+                     pinned_tiling, rel_l2, row_mask, sample_rows, upload)
 from synth.paging import page_layout, paged_copy
 
 pytestmark = pytest.mark.gpu
@@ -103,7 +103,7 @@ def test_random_case(i):
 
     # 1. sampled rows against the oracle
     rows = sample_rows(c.x, 12, seed=i)
-    C, Bk = K.get_tiling()
+    C, Bk = pinned_tiling()
     ref = oracle_decode(c, rows=rows, p_mode=d["p_mode"], C=C, Bk=Bk)
     m = row_mask(full.shape, rows)
     if d["p_mode"] == 0:

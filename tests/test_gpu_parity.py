@@ -11,8 +11,8 @@ import numpy as np
 import pytest
 
 import oracle
-from helpers import (ROUNDED_REL_L2, assert_f32_tolerance, custom, oracle_decode, rel_l2,
-                     row_mask, run, sample_rows, upload)
+from helpers import (ROUNDED_REL_L2, assert_f32_tolerance, bits, custom, oracle_decode,
+                     pinned_tiling, rel_l2, row_mask, run, sample_rows, upload)
 from synth import WORKLOADS, make_workload
 
 pytestmark = pytest.mark.gpu
@@ -22,10 +22,6 @@ pytestmark = pytest.mark.gpu
 def built():
     import __graft_entry__
     __graft_entry__.build()
-
-
-def bits(a):
-    return np.ascontiguousarray(np.asarray(a, np.float32)).view(np.uint32)
 
 
 # ----------------------------------------------------------- quantization --
@@ -116,7 +112,7 @@ def test_fast_f32_spec_verify_sampled():
 @pytest.mark.parametrize("name", ["tiny", "qwen_layer"])
 def test_fast_rounded_p_modes(name, p_mode):
     import int8_kv_decode_gb300 as K
-    C, Bk = K.get_tiling()
+    C, Bk = pinned_tiling()
     c = upload(WORKLOADS[name])
     got = run(c, p_mode=p_mode).cpu().numpy()
     same = oracle_decode(c, p_mode=p_mode, C=C, Bk=Bk)
@@ -195,7 +191,7 @@ def test_shape_sweep(g, M):
     # ctx around the block and split sizes ("海光 DCU 实测" §4: one shape being
     # exact proves nothing about the others).
     import int8_kv_decode_gb300 as K
-    C, Bk = K.get_tiling()
+    C, Bk = pinned_tiling()
     ctxs = np.array([1, 2, Bk - 1, Bk, Bk + 1, C - 1, C, C + 1, 2 * C + 3], np.int32)
     wl = custom(f"sweep_g{g}_m{M}", len(ctxs), M, 2 * g, 2, 1, outliers=True)
     c = upload(wl, ctx_override=ctxs)
@@ -295,74 +291,7 @@ def test_bad_sequence_is_flagged_without_touching_other_rows():
     torch.cuda.synchronize()
 
 
-# -------------------------------------------------------------- full size --
-
-def _device_case(name):
-    import torch
-    import int8_kv_decode_gb300 as K
-    wl = WORKLOADS[name]
-    x = make_workload(wl, device="cuda")
-    k8 = torch.empty((wl.Hkv, x.cap_rows, wl.d), dtype=torch.int8, device="cuda")
-    v8 = torch.empty_like(k8)
-    ks = torch.empty((wl.Hkv, x.cap_rows), dtype=torch.float32, device="cuda")
-    vs = torch.empty_like(ks)
-    K.quantize_kv(x.k_rows, k8, ks)
-    K.quantize_kv(x.v_rows, v8, vs)
-    return x, k8, ks, v8, vs
-
-
-def _oracle_one_sequence(x, b, rows, k8, ks, **kw):
-    """Oracle on sequence b alone, from the generator's float32 rows."""
-    lo, hi = x.rows_of(b)
-    kr = x.k_rows[lo:hi].cpu().numpy()
-    vr = x.v_rows[lo:hi].cpu().numpy()
-    ok8, oks = oracle.quant.quantize_kv(kr)
-    ov8, ovs = oracle.quant.quantize_kv(vr)
-    assert np.array_equal(k8[:, lo:hi].cpu().numpy(), ok8)      # quantization parity
-    assert np.array_equal(bits(ks[:, lo:hi].cpu().numpy()), bits(oks))
-    q = x.q[b:b + 1].cpu().numpy()
-    return oracle.attention.decode(q, ok8, oks, ov8, ovs, np.array([0]), x.ctx[b:b + 1],
-                                   rows=[(0, j, h) for (j, h) in rows], **kw)
-
-
-@pytest.mark.parametrize("p_mode", [0, 2])
-def test_full_size_long_context_sampled(p_mode):
-    import torch
-    import int8_kv_decode_gb300 as K
-    C, Bk = K.get_tiling()
-    x, k8, ks, v8, vs = _device_case("long_128k")
-    out = K.decode(x.q, k8, ks, v8, vs, torch.from_numpy(x.row_start).cuda(),
-                   torch.from_numpy(x.ctx).cuda(), x.max_ctx, p_mode=p_mode).cpu().numpy()
-    assert np.isfinite(out).all()
-    got, ref = [], []
-    for b, rows in ((0, [(0, 0), (0, 31)]), (3, [(0, 17)])):
-        o = _oracle_one_sequence(x, b, rows, k8, ks, p_mode=p_mode, C=C, Bk=Bk)
-        for (j, h) in rows:
-            got.append(out[b, j, h])
-            ref.append(o[0, j, h])
-    if p_mode == 0:
-        assert_f32_tolerance(np.array(got), np.array(ref))
-    else:
-        assert rel_l2(np.array(got), np.array(ref)) <= ROUNDED_REL_L2
-
-
-def test_full_size_serving_sampled():
-    import torch
-    import int8_kv_decode_gb300 as K
-    x, k8, ks, v8, vs = _device_case("serving_b256_m1")
-    out = K.decode(x.q, k8, ks, v8, vs, torch.from_numpy(x.row_start).cuda(),
-                   torch.from_numpy(x.ctx).cuda(), x.max_ctx).cpu().numpy()
-    assert np.isfinite(out).all()
-    got, ref = [], []
-    longest = int(np.argmax(x.ctx))
-    for b in (0, longest, 255):
-        rows = [(0, 0), (0, 31)]
-        o = _oracle_one_sequence(x, b, rows, k8, ks)
-        for (j, h) in rows:
-            got.append(out[b, j, h])
-            ref.append(o[0, j, h])
-    assert_f32_tolerance(np.array(got), np.array(ref))
-
+# ------------------------------------------------------------ fused append --
 
 @pytest.mark.parametrize("name,p_mode", [("spec_verify", 0), ("spec_verify", 2), ("qwen_layer", 0),
                                          ("r32", 0)])
@@ -460,7 +389,7 @@ def test_e4m3_direct_mode_columns_and_oracle():
     # the same rounding, every draft column equal to the M = 1 decode (the
     # mma.sync kernel) byte for byte, and no exact-mode form.
     import int8_kv_decode_gb300 as K
-    C, Bk = K.get_tiling()
+    C, Bk = pinned_tiling()
     wl = custom("direct_m4", 5, 4, 16, 2, ("uniform", 300, 2500), outliers=True, index=77)
     c = upload(wl)
     got = run(c, p_mode=5).cpu().numpy()

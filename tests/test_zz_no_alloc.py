@@ -49,6 +49,32 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(name):
         assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.gpu
+def test_noalloc_after_a_larger_call_leaks_nothing_into_a_smaller_one():
+    # The shared array keeps everything the previous call wrote: its work
+    # list, item count, packed queries and window partials.  A large call
+    # (16 sequences, 5 draft columns, up to 9 windows each) followed by small
+    # ones of another batch size, column count and GQA group must give the
+    # bytes of kattn_decode with a freshly zeroed workspace.
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    big = upload(WORKLOADS["spec_verify"])
+    small = [upload(custom("noalloc_small", 3, 1, 8, 2, ("uniform", 40, 1500), outliers=False)),
+             upload(custom("noalloc_small_r32", 2, 4, 16, 2, ("uniform", 600, 1100),
+                           outliers=True))]
+    out_big = torch.full_like(big.q, float("nan"))
+    assert _noalloc(big, out_big) == 0
+    for c in small + [small[0]]:
+        ref = run(c).cpu().numpy()              # fresh workspace, zeroed by torch
+        out = torch.full_like(c.q, float("nan"))
+        assert _noalloc(c, out) == 0
+        got = out.cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    ref_big = run(big).cpu().numpy()
+    assert np.array_equal(out_big.cpu().numpy().view(np.uint32), ref_big.view(np.uint32))
+
+
 def test_noalloc_rejects_requests_beyond_its_scratch():
     # Checked on the host before any CUDA call: the pointers are never used.
     import __graft_entry__
