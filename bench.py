@@ -2,8 +2,9 @@
 """Decode-attention benchmark: KV GB/s and queries/s on GB300, % of HBM roofline.
 
 One step = one decode step of the hot path over one batch of synthetic
-sequences: kattn_decode_append quantizes this step's appended K and V rows
-into the int8 cache and decodes every sequence, in one call.  The
+sequences: kattn_decode_append (kattn_decode_paged_append for the paged
+layout) quantizes this step's appended K and V rows into the int8 cache and
+decodes every sequence, in one call.  The
 default workload is the serving mix: 256 ragged sequences, contexts
 log-uniform in [512, 32768], 32 query / 4 KV heads, head_dim 128, M = 1,
 float32 P, fast mode.
@@ -430,14 +431,17 @@ def run_ours(args):
 
     def step(i):
         k8, ks, v8, vs = caches[i % n_copies]
-        if exact or P:
-            # exact mode and the paged layout have no fused append: the two
-            # appends, then the decode
+        if exact:
+            # exact mode has no fused append: the two appends, then the decode
             K.quantize_kv_rows(knew, dst, k8, ks)
             K.quantize_kv_rows(vnew, dst, v8, vs)
             decode(i)
             return
         # this step's K/V rows appended inside the decode call
+        if P:
+            K.decode_paged_append(q, knew, vnew, dst, k8, ks, v8, vs, bt, P, ctx, max_ctx,
+                                  out=out, workspace=ws, p_mode=pm)
+            return
         K.decode_append(q, knew, vnew, dst, k8, ks, v8, vs, rs, ctx, max_ctx, out=out,
                         workspace=ws, p_mode=pm)
 
@@ -596,8 +600,8 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": total_bytes / e_tmax / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": ((2 if exact or P else 0) +
-                         (1 if exact else K.decode_launch_count(B, M, Hq, Hkv, max_ctx))) * args.steps,
+        "gpu_launches": ((3 if exact else K.decode_launch_count(B, M, Hq, Hkv, max_ctx))
+                         * args.steps),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -232,6 +232,25 @@ int kattn_decode_append(const float* q, const float* k_new, const float* v_new,
                         int Hkv, int d, int cap_rows, int max_ctx, float sm_scale, int p_mode,
                         float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* kattn_decode_append over a paged cache: the step's K/V rows quantized into
+ * the pool and kattn_decode_paged in fast mode, in the same launches as
+ * kattn_decode_paged (the append rides in the query-packing launch).
+ * dst_rows are PHYSICAL rows of the pool, as for kattn_quantize_kv_rows: the
+ * caller maps key t of sequence b through its block table,
+ *   block_table[b * max_pages + t / page_rows] * page_rows + t % page_rows,
+ * and for the rows to be attended, t lies inside the keys a column sees
+ * (e.g. the M draft keys ctx_len[b] - 1 + j).  Out-of-range rows are skipped
+ * on the device.  The cache bytes and `out` equal, byte for byte, those of
+ * kattn_quantize_kv_rows twice followed by kattn_decode_paged.  Paging
+ * arguments as kattn_decode_paged; append arguments as kattn_decode_append. */
+int kattn_decode_paged_append(const float* q, const float* k_new, const float* v_new,
+                              const int64_t* dst_rows, int n_new, int64_t row_stride_elems,
+                              int8_t* k, float* k_scale, int8_t* v, float* v_scale,
+                              const int32_t* block_table, int max_pages, int page_rows,
+                              const int32_t* ctx_len, int B, int M, int Hq, int Hkv, int d,
+                              int cap_rows, int max_ctx, float sm_scale, int p_mode, float* out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------ context parallel -- */
 /* One sequence's keys spread over several GPUs (context parallelism): every
  * GPU reduces the 512-key windows it holds into window partials, the

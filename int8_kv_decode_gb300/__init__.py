@@ -12,6 +12,7 @@ from .api import (  # noqa: F401
     decode_append,
     decode_launch_count,
     decode_paged,
+    decode_paged_append,
     decode_shard,
     decode_workspace_size,
     expf_constants,

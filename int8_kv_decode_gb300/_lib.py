@@ -36,6 +36,11 @@ SIGNATURES = {
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
                                     c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "kattn_decode_paged_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int64,
+                                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                          c_int, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                          c_int, c_int, c_float, c_int, c_void_p, c_void_p,
+                                          c_size_t, c_void_p]),
     "kattn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                      c_int, c_int, c_float, c_int, c_void_p, c_void_p]),

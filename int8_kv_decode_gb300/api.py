@@ -233,6 +233,50 @@ def decode_append(q, k_new, v_new, dst_rows, k, k_scale, v, v_scale, row_start, 
     return out
 
 
+def decode_paged_append(q, k_new, v_new, dst_rows, k, k_scale, v, v_scale, block_table,
+                        page_rows: int, ctx_len, max_ctx: int, *, out=None, p_mode=0,
+                        sm_scale: float = 0.0, workspace=None):
+    """Append rows k_new / v_new [n][Hkv][d] f32 at PHYSICAL pool rows
+    dst_rows [n] (int64), then decode the paged cache (fast mode): one call of
+    kattn_decode_paged_append.  Paging arguments as decode_paged()."""
+    _need(q, torch.float32, "q", 4)
+    _need(k_new, torch.float32, "k_new", 3)
+    _need(v_new, torch.float32, "v_new", 3)
+    _need(dst_rows, torch.int64, "dst_rows", 1)
+    _need(k, torch.int8, "k", 3)
+    _need(v, torch.int8, "v", 3)
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(v_scale, torch.float32, "v_scale", 2)
+    _need(block_table, torch.int32, "block_table", 2)
+    _need(ctx_len, torch.int32, "ctx_len", 1)
+    B, M, Hq, d = q.shape
+    Hkv, cap, _ = k.shape
+    n_new = k_new.shape[0]
+    if tuple(v_new.shape) != tuple(k_new.shape) or dst_rows.numel() != n_new \
+            or k_new.shape[1] != Hkv or k_new.shape[2] != d:
+        raise ValueError("k_new / v_new / dst_rows shapes disagree with the cache")
+    if tuple(v.shape) != tuple(k.shape) or tuple(k_scale.shape) != (Hkv, cap) \
+            or tuple(v_scale.shape) != (Hkv, cap):
+        raise ValueError("k/v/scales shapes disagree")
+    if block_table.shape[0] != B or ctx_len.numel() != B:
+        raise ValueError("block_table / ctx_len must have B rows")
+    mode = P_MODES.get(p_mode, p_mode) if isinstance(p_mode, str) else int(p_mode)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, torch.float32, "out", 4)
+    if workspace is None:
+        workspace = alloc_workspace(B, M, Hq, max_ctx, q.device)
+    _need(workspace, torch.uint8, "workspace", 1)
+    lib = _lib.load()
+    _lib.check("kattn_decode_paged_append", lib.kattn_decode_paged_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(dst_rows), n_new, Hkv * d, _ptr(k), _ptr(k_scale),
+        _ptr(v), _ptr(v_scale), _ptr(block_table), int(block_table.shape[1]), int(page_rows),
+        _ptr(ctx_len), B, M, Hq, Hkv, d, cap, int(max_ctx), float(sm_scale), mode, _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(q.device)))
+    return out
+
+
 WINDOW_KEYS = 512   # KATTN_WINDOW_KEYS: keys per window, the unit of a shard
 
 

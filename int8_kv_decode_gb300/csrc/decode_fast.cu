@@ -336,6 +336,11 @@ bool encode_cache_map(CUtensorMap* map, const int8_t* base, int64_t rows) {
 cudaError_t launch_split_contiguous(const DecodeParams& p, const TmaMaps& maps,
                                     cudaStream_t stream) {
   if (p.R <= 8) return launch_modes<1, 1, false>(p, maps, stream);
+  if (const int nrg = row_groups_for(p); nrg > 1) {      // rows in groups of 8, a CTA each
+    DecodeParams pr = p;
+    pr.row_groups = nrg;
+    return launch_modes<1, 1, false>(pr, maps, stream);
+  }
   if (p.R <= 16) return launch_modes<2, 1, false>(p, maps, stream);
   if (p.R <= 32) return launch_split_tc(p, maps, stream);   // P.V on tcgen05
   if (p.R <= 48) return launch_modes<3, 2, false>(p, maps, stream);

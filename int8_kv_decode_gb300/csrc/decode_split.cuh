@@ -132,6 +132,13 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
   return pol;
 }
+// With row groups the K/V of a window is read by several CTAs: keep it in L2
+// at normal priority until they have all read it.
+__device__ __forceinline__ uint64_t l2_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
 
 // kBlockBk rows x 128 bytes starting at row `row` of a 2-D cache view.
 __device__ __forceinline__ void tma_load_block(void* dst, const CUtensorMap* map, int row,
@@ -280,14 +287,27 @@ __device__ __forceinline__ void named_arrive(int id, int threads) {
 // key's row from the block table.  b < 0 marks "no item".
 struct Item {
   int b, kh, w, row, ctx;
+  int rg;               // row group: rows [8 rg, 8 rg + 8) of the item (row-group split)
 };
 
 __device__ __forceinline__ Item load_item(const DecodeParams& p, int t, int total) {
-  Item it{-1, 0, 0, 0, 0};
+  Item it{-1, 0, 0, 0, 0, 0};
   if (t < total) {
     const int4 v = __ldcg(p.items + t);
-    it = Item{v.x & 0xffff, (int)((unsigned)v.x >> 16), v.y, v.z, v.w};
+    it = Item{v.x & 0xffff, (int)((unsigned)v.x >> 16), v.y, v.z, v.w, 0};
   }
+  return it;
+}
+
+// Unit t of the decode grid when every work item is split into nrg row
+// groups (nrg > 1: the one-tile kernel, 8 query rows per CTA): item t / nrg,
+// row group t % nrg.  The row groups of an item are consecutive units, so
+// CTAs that run side by side read the same K/V blocks, the later ones from L2.
+__device__ __forceinline__ Item load_unit(const DecodeParams& p, int t, int total, int nrg) {
+  if (nrg == 1) return load_item(p, t, total);
+  const int i = t / nrg;
+  Item it = load_item(p, i, total);
+  it.rg = t - i * nrg;
   return it;
 }
 
@@ -356,24 +376,34 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   const int kw = warp % kSpansPerCta, grp = warp / kSpansPerCta;
   const int g = lane >> 2, c = lane & 3;
   const int gq = p.g, M = p.M, R = p.R;
-  const int row0 = grp * RG;
+  // Row groups (one-tile kernel only): an item's R rows are split over
+  // nrg = ceil(R / 8) units of 8 rows, one CTA each.  The CTA then holds
+  // rows [8 rg, 8 rg + 8) of the item, at rows 0..7 of its query buffer.
+  constexpr bool kCanSplit = NR == 1 && NG == 1;
+  const int nrg = kCanSplit ? p.row_groups : 1;
+  const int qrow0 = grp * RG;                     // the group's first row in qbuf
   // Span kw's ring is filled by warp kw of group 0 and read by warp kw of
   // every group (the groups hold different query rows).
   uint64_t* full = sm.full[kw];
   uint64_t* empty = sm.empty[kw];
   const bool producer = grp == 0;
-  // Per thread and fixed for the launch: the draft column j of rows
-  // 8nr + 2c + e of the group, and where those rows sit in out (head kh * g
-  // + r % g; add kh * g * d and the sequence's offset).
+  // Per thread and item: the first row of the group (row0), the draft column
+  // j of rows row0 + 8nr + 2c + e, and where those rows sit in out (head
+  // kh * g + r % g; add kh * g * d and the sequence's offset).
+  int row0 = qrow0;
   int jrow[NR][2], orow[NR][2];
+  auto place_rows = [&](int rg) {
+    row0 = qrow0 + 8 * rg;
 #pragma unroll
-  for (int nr = 0; nr < NR; ++nr)
+    for (int nr = 0; nr < NR; ++nr)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int r = row0 + nr * 8 + 2 * c + e;
-      jrow[nr][e] = min(r / gq, M - 1);
-      orow[nr][e] = ((r / gq) * p.Hq + r % gq) * kD + 16 * g;
-    }
+      for (int e = 0; e < 2; ++e) {
+        const int r = row0 + nr * 8 + 2 * c + e;
+        jrow[nr][e] = min(r / gq, M - 1);
+        orow[nr][e] = ((r / gq) * p.Hq + r % gq) * kD + 16 * g;
+      }
+  };
+  place_rows(0);
 
   if (lane == 0 && producer) {
     for (int s = 0; s < kRing; ++s) {
@@ -391,17 +421,26 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   griddep_launch_dependents();
 
   const int total = (int)__ldcg(p.item_count);
+  const int units = total * nrg;                  // below 2^31: checked on the host
   const int G = gridDim.x;
   int t = blockIdx.x;
-  if (t >= total) return;
-  Item it0 = load_item(p, t, total), it1 = load_item(p, t + G, total),
-       it2 = load_item(p, t + 2 * G, total);
+  if (t >= units) return;
+  Item it0 = load_unit(p, t, total, nrg), it1 = load_unit(p, t + G, total, nrg),
+       it2 = load_unit(p, t + 2 * G, total, nrg);
+  if (nrg > 1) place_rows(it0.rg);
 
   bool q_pending = false;                         // thread 0: a query copy in flight
   auto fetch_queries = [&](const Item& it) {      // thread 0
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     mbar_expect_tx(&sm.qbar, kQBytes);
-    bulk_load(sm.qbuf, p.qpack + ((size_t)it.b * p.Hkv + it.kh) * kQBytes, kQBytes, &sm.qbar);
+    const uint8_t* pack = p.qpack + ((size_t)it.b * p.Hkv + it.kh) * qpack_bytes(p.rpad);
+    if (kCanSplit && nrg > 1) {
+      // the group's 8 int8 rows, then its 8 scales (the pack holds rpad rows)
+      bulk_load(sm.qbuf, pack + (size_t)it.rg * 8 * kD, 8 * kD, &sm.qbar);
+      bulk_load(sm.qbuf + 8 * kD, pack + (size_t)p.rpad * kD + it.rg * 8 * 4, 8 * 4, &sm.qbar);
+    } else {
+      bulk_load(sm.qbuf, pack, kQBytes, &sm.qbar);
+    }
     q_pending = true;
   };
   if (tid == 0) fetch_queries(it0);
@@ -426,7 +465,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   block_rows(it0, 0);
   block_rows(it1, 1);
   uint32_t used = 0, eph = 0;                     // NG > 1: stages filled before; empty parities
-  const uint64_t kv_policy = l2_evict_first();
+  const uint64_t kv_policy = nrg > 1 ? l2_evict_normal() : l2_evict_first();
   // Returns false if a stage was never released (a bounded wait ran out).
   auto produce = [&]() -> bool {
     if (!producer) return true;
@@ -481,14 +520,14 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     // fragments, and the sums are integers, so both are exact.
     uint32_t qw8[8];
     if constexpr (kQK8) {
-      const uint4* src = reinterpret_cast<const uint4*>(&sm.qbuf[(row0 + g) * kD + 32 * c]);
+      const uint4* src = reinterpret_cast<const uint4*>(&sm.qbuf[(qrow0 + g) * kD + 32 * c]);
       const uint4 lo = src[0], hi = src[1];
       qw8[0] = lo.x; qw8[1] = lo.y; qw8[2] = lo.z; qw8[3] = lo.w;
       qw8[4] = hi.x; qw8[5] = hi.y; qw8[6] = hi.z; qw8[7] = hi.w;
     } else {
       if (kw < NR) {                              // warp kw builds n-tile kw of its group
         const uint4* src =
-            reinterpret_cast<const uint4*>(&sm.qbuf[(row0 + kw * 8 + g) * kD + 32 * c]);
+            reinterpret_cast<const uint4*>(&sm.qbuf[(qrow0 + kw * 8 + g) * kD + 32 * c]);
         const uint4 lo = src[0], hi = src[1];
         const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
@@ -505,7 +544,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 #pragma unroll
       for (int nr = 0; nr < NR; ++nr)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) qs_row[nr][e] = qsb[row0 + nr * 8 + 2 * c + e];
+        for (int e = 0; e < 2; ++e) qs_row[nr][e] = qsb[qrow0 + nr * 8 + 2 * c + e];
     }
 
     // Power of two 2^E per query row: over the keys of the span that the row
@@ -900,10 +939,11 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
 
     // ---- next item
     t += G;
-    if (t >= total) break;
+    if (t >= units) break;
     it0 = it1;
     it1 = it2;
-    it2 = load_item(p, t + 2 * G, total);
+    it2 = load_unit(p, t + 2 * G, total, nrg);
+    if (nrg > 1) place_rows(it0.rg);
     sp = span_of(it0, kw, M);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -967,9 +1007,27 @@ cudaError_t launch_variant(const DecodeParams& p, const TmaMaps& maps, cudaStrea
     slots = sms * (per_sm > 0 ? per_sm : 1);
     if (dev >= 0 && dev < kMaxDevices) slots_cache[dev].store(slots);
   }
-  const int64_t items = (int64_t)p.B * p.nsplit_max * p.Hkv;   // an upper bound
-  const int grid = (int)(items < slots ? items : slots);
+  const int64_t units = (int64_t)p.B * p.nsplit_max * p.Hkv * p.row_groups;   // an upper bound
+  const int grid = (int)(units < slots ? units : slots);
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), (size_t)smem, stream, p, maps);
+}
+
+// Row groups.  With more than 8 query rows per (sequence, kv head), the rows
+// of a work item can be split into groups of 8, each reduced by its own CTA
+// of the one-tile kernel (int8 QK, the M = 1 per-row arithmetic, so the bytes
+// of every row are unchanged); the K/V of the item is then read from L2 by
+// all but the first group.  That pays where the grouped kernels would leave
+// the GPU short of work: a small batch, with about as many items as CTA slots
+// (speculative verify).  With many items the grouped kernels, which read
+// each K/V block once into shared memory for all rows, are kept.
+constexpr int64_t kRowGroupMaxItems = 4096;       // upper bound on items for the split
+
+inline int row_groups_for(const DecodeParams& p) {
+  if (p.R <= 8) return 1;
+  const int64_t items = (int64_t)p.B * p.nsplit_max * p.Hkv;
+  const int nrg = (p.R + 7) / 8;
+  if (items > kRowGroupMaxItems || items * nrg > (int64_t)INT32_MAX / 4) return 1;
+  return nrg;
 }
 
 template <int NR, int NG, bool PG>

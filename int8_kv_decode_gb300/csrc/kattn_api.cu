@@ -60,6 +60,7 @@ DecodeParams make_params(const float* q, const int8_t* k, const float* k_scale,
   p.g = Hq / Hkv;
   p.R = p.g * M;
   p.rpad = row_tile(p.R);
+  p.row_groups = 1;
   p.cap_rows = cap_rows;
   p.max_ctx = max_ctx;
   p.nsplit_max = nsplit_for(max_ctx + M - 1);
@@ -107,6 +108,65 @@ void set_workspace(DecodeParams& p, const WorkspaceLayout& w, void* workspace) {
   p.items = reinterpret_cast<int4*>(ws + w.items_off);
   p.qpack = ws + w.q_off;
   p.partials = reinterpret_cast<float*>(ws + w.partials_off);
+}
+
+// The paged layout's own argument rules, and its fields of p.
+int check_paging(int max_pages, int page_rows, int cap_rows) {
+  if (max_pages < 1 || page_rows < 1) return KATTN_ERR_INVALID_ARG;
+  // a TMA block of 32 keys must lie inside one page
+  if (page_rows < kBlockBk || (page_rows & (page_rows - 1)) != 0) return KATTN_ERR_UNSUPPORTED;
+  if (cap_rows % page_rows != 0) return KATTN_ERR_INVALID_ARG;
+  return KATTN_OK;
+}
+
+void set_paging(DecodeParams& p, const int32_t* block_table, int max_pages, int page_rows,
+                int cap_rows) {
+  p.block_table = block_table;
+  p.max_pages = max_pages;
+  p.page_shift = __builtin_ctz((unsigned)page_rows);
+  p.n_pages = cap_rows / page_rows;
+}
+
+// The append and the decode of kattn_decode_append / kattn_decode_paged_append,
+// once the layout's own checks are done and p holds the layout: the append
+// rides in the decode's query-packing launch (fast mode).
+int run_append(DecodeParams& p, const float* k_new, const float* v_new, const int64_t* dst_rows,
+               int n_new, int64_t row_stride_elems, int8_t* k, float* k_scale, int8_t* v,
+               float* v_scale, int p_mode, float sm_scale, float* out, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_DIRECT) return KATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
+  if (n_new < 0 || row_stride_elems < (int64_t)p.Hkv * kD) return KATTN_ERR_INVALID_ARG;
+  if (n_new > 0 && (!k_new || !v_new || !dst_rows)) return KATTN_ERR_INVALID_ARG;
+  if (n_new > 0 && (!aligned(k_new, 16) || !aligned(v_new, 16) || row_stride_elems % 4 != 0 ||
+                    !aligned(dst_rows, 8)))
+    return KATTN_ERR_MISALIGNED;
+  if (p.B == 0) {                                 // nothing to decode: the append alone
+    if (n_new == 0) return KATTN_OK;
+    int e = kattn_quantize_kv_rows(k_new, n_new, p.Hkv, kD, row_stride_elems, dst_rows, k, k_scale,
+                                   p.cap_rows, stream);
+    if (e != KATTN_OK) return e;
+    return kattn_quantize_kv_rows(v_new, n_new, p.Hkv, kD, row_stride_elems, dst_rows, v, v_scale,
+                                  p.cap_rows, stream);
+  }
+  if (!v || !v_scale || !out) return KATTN_ERR_INVALID_ARG;
+  if (!aligned(v, 16) || !aligned(v_scale, 4) || !aligned(out, 16)) return KATTN_ERR_MISALIGNED;
+  const WorkspaceLayout w = workspace_layout(p.B, p.M, p.Hq, p.max_ctx);
+  if ((int64_t)p.B * w.nsplit_max * p.Hkv > (int64_t)INT32_MAX / 4) return KATTN_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
+    return KATTN_ERR_WORKSPACE;
+  set_workspace(p, w, workspace);
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.dst_rows = dst_rows;
+  p.n_new = n_new;
+  p.new_stride = row_stride_elems;
+  p.k_w = k;
+  p.ks_w = k_scale;
+  p.v_w = v;
+  p.vs_w = v_scale;
+  const cudaError_t e = launch_decode_fast(p, as_stream(stream));
+  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
 }
 
 }  // namespace
@@ -202,16 +262,11 @@ int kattn_decode_paged(const float* q, const int8_t* k, const float* k_scale, co
   int st = check_common(q, k, k_scale, block_table, 4, ctx_len, B, M, Hq, Hkv, d, cap_rows,
                         max_ctx);
   if (st != KATTN_OK) return st;
-  if (max_pages < 1 || page_rows < 1) return KATTN_ERR_INVALID_ARG;
-  // a TMA block of 32 keys must lie inside one page
-  if (page_rows < kBlockBk || (page_rows & (page_rows - 1)) != 0) return KATTN_ERR_UNSUPPORTED;
-  if (cap_rows % page_rows != 0) return KATTN_ERR_INVALID_ARG;
+  st = check_paging(max_pages, page_rows, cap_rows);
+  if (st != KATTN_OK) return st;
   DecodeParams p = make_params(q, k, k_scale, v, v_scale, nullptr, ctx_len, B, M, Hq, Hkv,
                                cap_rows, max_ctx, sm_scale, p_mode, out);
-  p.block_table = block_table;
-  p.max_pages = max_pages;
-  p.page_shift = __builtin_ctz((unsigned)page_rows);
-  p.n_pages = cap_rows / page_rows;
+  set_paging(p, block_table, max_pages, page_rows, cap_rows);
   return run_decode(p, p_mode, exact_mode, sm_scale, v, v_scale, out, workspace, workspace_bytes,
                     stream);
 }
@@ -224,41 +279,29 @@ int kattn_decode_append(const float* q, const float* k_new, const float* v_new,
                         void* workspace, size_t workspace_bytes, void* stream) {
   int st = check_common(q, k, k_scale, row_start, 8, ctx_len, B, M, Hq, Hkv, d, cap_rows, max_ctx);
   if (st != KATTN_OK) return st;
-  if (p_mode < KATTN_P_F32 || p_mode > KATTN_P_E4M3_DIRECT) return KATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(sm_scale)) return KATTN_ERR_INVALID_ARG;
-  if (n_new < 0 || row_stride_elems < (int64_t)Hkv * d) return KATTN_ERR_INVALID_ARG;
-  if (n_new > 0 && (!k_new || !v_new || !dst_rows)) return KATTN_ERR_INVALID_ARG;
-  if (n_new > 0 && (!aligned(k_new, 16) || !aligned(v_new, 16) || row_stride_elems % 4 != 0 ||
-                    !aligned(dst_rows, 8)))
-    return KATTN_ERR_MISALIGNED;
-  if (B == 0) {                                   // nothing to decode: the append alone
-    if (n_new == 0) return KATTN_OK;
-    int e = kattn_quantize_kv_rows(k_new, n_new, Hkv, d, row_stride_elems, dst_rows, k, k_scale,
-                                   cap_rows, stream);
-    if (e != KATTN_OK) return e;
-    return kattn_quantize_kv_rows(v_new, n_new, Hkv, d, row_stride_elems, dst_rows, v, v_scale,
-                                  cap_rows, stream);
-  }
-  if (!v || !v_scale || !out) return KATTN_ERR_INVALID_ARG;
-  if (!aligned(v, 16) || !aligned(v_scale, 4) || !aligned(out, 16)) return KATTN_ERR_MISALIGNED;
   DecodeParams p = make_params(q, k, k_scale, v, v_scale, row_start, ctx_len, B, M, Hq, Hkv,
                                cap_rows, max_ctx, sm_scale, p_mode, out);
-  const WorkspaceLayout w = workspace_layout(B, M, Hq, max_ctx);
-  if ((int64_t)B * w.nsplit_max * Hkv > (int64_t)INT32_MAX / 4) return KATTN_ERR_UNSUPPORTED;
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total)
-    return KATTN_ERR_WORKSPACE;
-  set_workspace(p, w, workspace);
-  p.k_new = k_new;
-  p.v_new = v_new;
-  p.dst_rows = dst_rows;
-  p.n_new = n_new;
-  p.new_stride = row_stride_elems;
-  p.k_w = k;
-  p.ks_w = k_scale;
-  p.v_w = v;
-  p.vs_w = v_scale;
-  cudaError_t e = launch_decode_fast(p, as_stream(stream));
-  return e == cudaSuccess ? KATTN_OK : KATTN_ERR_CUDA;
+  return run_append(p, k_new, v_new, dst_rows, n_new, row_stride_elems, k, k_scale, v, v_scale,
+                    p_mode, sm_scale, out, workspace, workspace_bytes, stream);
+}
+
+int kattn_decode_paged_append(const float* q, const float* k_new, const float* v_new,
+                              const int64_t* dst_rows, int n_new, int64_t row_stride_elems,
+                              int8_t* k, float* k_scale, int8_t* v, float* v_scale,
+                              const int32_t* block_table, int max_pages, int page_rows,
+                              const int32_t* ctx_len, int B, int M, int Hq, int Hkv, int d,
+                              int cap_rows, int max_ctx, float sm_scale, int p_mode, float* out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_common(q, k, k_scale, block_table, 4, ctx_len, B, M, Hq, Hkv, d, cap_rows,
+                        max_ctx);
+  if (st != KATTN_OK) return st;
+  st = check_paging(max_pages, page_rows, cap_rows);
+  if (st != KATTN_OK) return st;
+  DecodeParams p = make_params(q, k, k_scale, v, v_scale, nullptr, ctx_len, B, M, Hq, Hkv,
+                               cap_rows, max_ctx, sm_scale, p_mode, out);
+  set_paging(p, block_table, max_pages, page_rows, cap_rows);
+  return run_append(p, k_new, v_new, dst_rows, n_new, row_stride_elems, k, k_scale, v, v_scale,
+                    p_mode, sm_scale, out, workspace, workspace_bytes, stream);
 }
 
 int kattn_qk_scores_debug(const float* q, const int8_t* k, const float* k_scale,

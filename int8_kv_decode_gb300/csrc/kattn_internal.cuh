@@ -92,6 +92,8 @@ struct DecodeParams {
   float* partials;
   int B, M, Hq, Hkv, g, R;
   int rpad;             // row_tile(R)
+  int row_groups;       // > 1: every work item split into this many units of
+                        // 8 query rows, one CTA each (the one-tile kernel)
   int list_blocks;      // > 0: prepare_kernel writes the work items in this many blocks
   // Rows appended before the decode (kattn_decode_append), n_new = 0 if none:
   // row r of k_new / v_new goes to cache row dst_rows[r] of every kv head.

@@ -140,6 +140,34 @@ def test_decode_paged_validation(lib):
     assert _decode_paged(lib, B=0) == 0
 
 
+def _paged_append(lib, **kw):
+    a = dict(q=64, kn=64, vn=64, dst=64, n=2, stride=256, k=64, ks=64, v=64, vs=64, bt=64,
+             max_pages=8, page=32, ctx=64, B=1, M=1, Hq=8, Hkv=2, d=128, cap=256, max_ctx=256,
+             sm=0.0, p_mode=0, out=64, ws=0, ws_bytes=0, stream=0)
+    a.update(kw)
+    return lib.kattn_decode_paged_append(
+        a["q"], a["kn"], a["vn"], a["dst"], a["n"], a["stride"], a["k"], a["ks"], a["v"],
+        a["vs"], a["bt"], a["max_pages"], a["page"], a["ctx"], a["B"], a["M"], a["Hq"], a["Hkv"],
+        a["d"], a["cap"], a["max_ctx"], a["sm"], a["p_mode"], a["out"], a["ws"], a["ws_bytes"],
+        a["stream"])
+
+
+def test_decode_paged_append_validation(lib):
+    # Checked on the host before any CUDA call: the pointers are never used.
+    INVALID, UNSUP, MISAL, WS = -1, -2, -3, -4
+    assert _paged_append(lib, page=16) == UNSUP
+    assert _paged_append(lib, page=64, cap=224) == INVALID
+    assert _paged_append(lib, bt=0x1002) == MISAL
+    assert _paged_append(lib, n=-1) == INVALID
+    assert _paged_append(lib, stride=255) == INVALID          # < Hkv * d
+    assert _paged_append(lib, kn=0) == INVALID
+    assert _paged_append(lib, dst=0x1004) == MISAL            # int64 rows
+    assert _paged_append(lib, stride=258) == MISAL
+    assert _paged_append(lib, p_mode=6) == INVALID
+    assert _paged_append(lib, ws=0) == WS
+    assert _paged_append(lib, B=0, n=0) == 0                  # nothing at all: no-op
+
+
 def test_quantize_validation(lib):
     f = lib.kattn_quantize_kv
     assert f(64, 4, 2, 64, 256, 64, 64, 0, 8, 0) == -2       # d != 128

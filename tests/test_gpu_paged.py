@@ -126,3 +126,54 @@ def test_paged_bad_tables_are_flagged_without_touching_other_sequences(M, Hq):
     assert np.isfinite(out[[1, 4]]).all()
     assert K.get_device_status(ws) == 4          # KATTN_DEVERR_BAD_PAGE
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name,P,p_mode", [("spec_verify", 32, 0), ("spec_verify", 64, 3),
+                                           ("qwen_layer", 128, 0)])
+def test_paged_append_equals_separate_calls_and_the_oracle(name, P, p_mode):
+    # kattn_decode_paged_append: the step's K/V rows quantized into the pool at
+    # the physical rows of each sequence's M newest keys, then the paged
+    # decode, in one launch chain.  The same bytes as the two row appends and
+    # kattn_decode_paged; the oracle quantizes the rows itself and decodes its
+    # contiguous copy of the cache.
+    import torch
+    import int8_kv_decode_gb300 as K
+    import oracle
+    from helpers import ROUNDED_REL_L2, assert_f32_tolerance, pinned_tiling, rel_l2
+    C, Bk = pinned_tiling()
+    c = upload(WORKLOADS[name], rep=3)
+    wl, x = c.x.wl, c.x
+    fused, separate = Paged(c, P, seed=5), Paged(c, P, seed=5)
+    seqs = np.repeat(np.arange(wl.B), wl.M)
+    keys = np.concatenate([np.arange(int(n) - 1, int(n) - 1 + wl.M) for n in x.ctx])
+    bt = fused.layout.block_table
+    phys = bt[seqs, keys // P].astype(np.int64) * P + keys % P
+    fresh = make_workload(wl, rep=4)
+    knew = np.ascontiguousarray(fresh.k_rows[:len(phys)])
+    vnew = np.ascontiguousarray(fresh.v_rows[:len(phys)])
+    tk, tv = torch.from_numpy(knew).cuda(), torch.from_numpy(vnew).cuda()
+    dst = torch.from_numpy(phys).cuda()
+    ws = K.alloc_workspace(wl.B, wl.M, wl.Hq, x.max_ctx)
+    got = K.decode_paged_append(c.q, tk, tv, dst, fused.k8, fused.ks, fused.v8, fused.vs,
+                                fused.bt, P, c.ctx, x.max_ctx, p_mode=p_mode,
+                                workspace=ws).cpu().numpy()
+    assert K.get_device_status(ws) == 0
+    K.quantize_kv_rows(tk, dst, separate.k8, separate.ks)
+    K.quantize_kv_rows(tv, dst, separate.v8, separate.vs)
+    ref = separate.decode(c, p_mode=p_mode).cpu().numpy()
+    assert np.array_equal(bits(got), bits(ref))
+    for a, b in ((fused.k8, separate.k8), (fused.ks, separate.ks), (fused.v8, separate.v8),
+                 (fused.vs, separate.vs)):
+        assert torch.equal(a, b)
+    # the oracle: its own contiguous cache with the new rows at the same keys
+    ok8, oks, ov8, ovs = c.ok8.copy(), c.oks.copy(), c.ov8.copy(), c.ovs.copy()
+    rows = x.row_start[seqs] + keys
+    nk8, nks = oracle.quant.quantize_kv(knew)
+    nv8, nvs = oracle.quant.quantize_kv(vnew)
+    ok8[:, rows], oks[:, rows], ov8[:, rows], ovs[:, rows] = nk8, nks, nv8, nvs
+    want = oracle.attention.decode(x.q, ok8, oks, ov8, ovs, x.row_start, x.ctx, p_mode=p_mode,
+                                   C=C, Bk=Bk)
+    if p_mode == 0:
+        assert_f32_tolerance(got, want)
+    else:
+        assert rel_l2(got, want) <= ROUNDED_REL_L2
