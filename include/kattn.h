@@ -80,8 +80,11 @@ enum kattn_p_mode {
 
 /* Device error bits reported by kattn_get_device_status. */
 #define KATTN_DEVERR_BAD_SEQUENCE 0x1u /* row_start / ctx_len out of range */
-#define KATTN_DEVERR_TIMEOUT 0x2u      /* a bounded wait for a K/V block ran out;
-                                          the affected outputs are not written */
+#define KATTN_DEVERR_TIMEOUT 0x2u      /* a bounded wait inside a kernel ran out
+                                          (a K/V copy, or exact mode's hand-off
+                                          between its two thread groups); the
+                                          affected outputs are not written (fast
+                                          mode) or are NaN (exact mode) */
 #define KATTN_DEVERR_BAD_PAGE 0x4u     /* kattn_decode_paged: a block-table entry
                                           outside [0, cap_rows / page_rows) */
 
@@ -160,8 +163,9 @@ int kattn_quantize_kv_rows(const float* x, int n_rows, int n_kv, int d,
  *            <= max_ctx, with row_start[b] + ctx_len[b] + M - 1 <= cap_rows.
  *            These two arrays live on the device, so they are checked on the
  *            device: a sequence that breaks the rule gets NaN outputs and sets
- *            KATTN_DEVERR_BAD_SEQUENCE in the workspace (exact mode: no flag,
- *            NaN outputs only); no memory outside the arrays is touched.
+ *            KATTN_DEVERR_BAD_SEQUENCE in the workspace (exact mode: in the
+ *            workspace if one is given); no memory outside the arrays is
+ *            touched.
  * max_ctx:   host-side upper bound on ctx_len (sizes the grid).
  * sm_scale:  0 selects RN_f32(1/sqrt(d)).
  * p_mode:    a kattn_p_mode (KATTN_P_E4M3_DIRECT with exact_mode = 1 ->
@@ -180,7 +184,11 @@ int kattn_quantize_kv_rows(const float* x, int n_rows, int n_kv, int d,
  *   operation rounded separately (no contraction); exp by the table-driven
  *   method of "Kestrel_VLLM - 18" §3.3 (64-entry 2^(j/64) table, 3-term
  *   polynomial, double fused multiply-adds).  Bit-exact against the CPU
- *   oracle's sequential emulation.  workspace may be NULL.
+ *   oracle's sequential emulation.  workspace may be NULL; if given (at
+ *   least 256 bytes, 256-byte aligned, zeroed before its first use) only its
+ *   error word is used: KATTN_DEVERR_BAD_SEQUENCE, and KATTN_DEVERR_TIMEOUT
+ *   when a bounded hand-off wait between the kernel's two thread groups ran
+ *   out (that row's output is then NaN).
  * out:       float32 [B][M][Hq][d]. */
 int kattn_decode(const float* q, const int8_t* k, const float* k_scale,
                  const int8_t* v, const float* v_scale, const int64_t* row_start,

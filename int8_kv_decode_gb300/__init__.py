@@ -5,6 +5,9 @@ in include/kattn.h); this package is a thin torch-facing binding.
 """
 
 from .api import (  # noqa: F401
+    DEVERR_BAD_PAGE,
+    DEVERR_BAD_SEQUENCE,
+    DEVERR_TIMEOUT,
     P_MODES,
     WINDOW_KEYS,
     alloc_workspace,

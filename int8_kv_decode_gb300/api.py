@@ -15,6 +15,11 @@ from . import _lib
 
 P_MODES = {"f32": 0, "bf16": 1, "e4m3": 2, "e4m3x448": 3, "e4m3x256": 4, "e4m3direct": 5}
 
+# Device error bits (KATTN_DEVERR_* in kattn.h), as get_device_status returns them.
+DEVERR_BAD_SEQUENCE = 0x1
+DEVERR_TIMEOUT = 0x2
+DEVERR_BAD_PAGE = 0x4
+
 
 def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
@@ -115,7 +120,8 @@ def decode(q, k, k_scale, v, v_scale, row_start, ctx_len, max_ctx: int, *,
     "e4m3x256", or "e4m3direct" (e4m3 P fed straight to the P.V MMA as one
     f16 operand p~ * v_scale; fast mode only).
     workspace: a zeroed uint8 tensor of decode_workspace_size(...) bytes
-    (fast mode); allocated here with torch if None.
+    (fast mode); allocated here with torch if None.  Exact mode needs none; a
+    zeroed one of at least 256 bytes, if given, receives the device error bits.
     """
     _need(q, torch.float32, "q", 4)
     _need(k, torch.int8, "k", 3)
@@ -137,16 +143,16 @@ def decode(q, k, k_scale, v, v_scale, row_start, ctx_len, max_ctx: int, *,
     else:
         _need(out, torch.float32, "out", 4)
     ws_bytes = 0
-    if not exact_mode:
-        if workspace is None:
-            workspace = alloc_workspace(B, M, Hq, max_ctx, q.device)
+    if not exact_mode and workspace is None:
+        workspace = alloc_workspace(B, M, Hq, max_ctx, q.device)
+    if workspace is not None:                 # exact mode: optional, for the error word
         _need(workspace, torch.uint8, "workspace", 1)
         ws_bytes = workspace.numel()
     lib = _lib.load()
     _lib.check("kattn_decode", lib.kattn_decode(
         _ptr(q), _ptr(k), _ptr(k_scale), _ptr(v), _ptr(v_scale), _ptr(row_start), _ptr(ctx_len),
         B, M, Hq, Hkv, d, cap, int(max_ctx), float(sm_scale), mode, 1 if exact_mode else 0,
-        _ptr(out), _ptr(workspace) if not exact_mode else 0, ws_bytes, _stream(q.device)))
+        _ptr(out), _ptr(workspace), ws_bytes, _stream(q.device)))
     return out
 
 
@@ -179,9 +185,9 @@ def decode_paged(q, k, k_scale, v, v_scale, block_table, page_rows: int, ctx_len
     else:
         _need(out, torch.float32, "out", 4)
     ws_bytes = 0
-    if not exact_mode:
-        if workspace is None:
-            workspace = alloc_workspace(B, M, Hq, max_ctx, q.device)
+    if not exact_mode and workspace is None:
+        workspace = alloc_workspace(B, M, Hq, max_ctx, q.device)
+    if workspace is not None:                 # exact mode: optional, for the error word
         _need(workspace, torch.uint8, "workspace", 1)
         ws_bytes = workspace.numel()
     lib = _lib.load()
@@ -189,7 +195,7 @@ def decode_paged(q, k, k_scale, v, v_scale, block_table, page_rows: int, ctx_len
         _ptr(q), _ptr(k), _ptr(k_scale), _ptr(v), _ptr(v_scale), _ptr(block_table),
         int(block_table.shape[1]), int(page_rows), _ptr(ctx_len), B, M, Hq, Hkv, d, cap,
         int(max_ctx), float(sm_scale), mode, 1 if exact_mode else 0, _ptr(out),
-        _ptr(workspace) if not exact_mode else 0, ws_bytes, _stream(q.device)))
+        _ptr(workspace), ws_bytes, _stream(q.device)))
     return out
 
 

@@ -33,6 +33,7 @@ SOURCES = {
     "decode_fast.cu": [],
     "decode_fast_paged.cu": [],
     "decode_tc.cu": [],
+    "decode_tcw.cu": [],
     "decode_noalloc.cu": [],
     "decode_exact.cu": ["--fmad=false"],
     "expf_constants.cu": ["--fmad=false"],
@@ -105,6 +106,32 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         for out in outputs:
             print(out)
     return LIB
+
+
+# Test-only build: exact mode's hand-off waits give up after this many polls
+# (0: at once), so that a test can check the give-up path -- NaN rows and the
+# KATTN_DEVERR_TIMEOUT bit -- with no wait that could block.  Never loaded by
+# the package; only tests/test_gpu_exact_timeout.py loads it.
+TIMEOUT_VARIANT_LIB = os.path.join(BUILD, "libkattn_exact_spin0.so")
+
+
+def build_exact_timeout_variant(verbose: bool = False) -> str:
+    """libkattn.so with decode_exact.cu built with KATTN_EXACT_SPIN_LIMIT = 0
+    (every other object shared with the library); returns its path."""
+    build(verbose=verbose)
+    nvcc = nvcc_path()
+    src = os.path.join(CSRC, "decode_exact.cu")
+    obj = os.path.join(BUILD, "decode_exact_spin0.o")
+    deps = [src, __file__] + _headers()
+    if _stale(obj, deps):
+        _run([nvcc, "-c", src, "-o", obj] + ARCH + COMMON + SOURCES["decode_exact.cu"]
+             + ["-DKATTN_EXACT_SPIN_LIMIT=0u"], verbose)
+    objs = [os.path.join(BUILD, f.replace(".cu", ".o")) for f in SOURCES if f != "decode_exact.cu"]
+    if _stale(TIMEOUT_VARIANT_LIB, objs + [obj]):
+        tmp = TIMEOUT_VARIANT_LIB + ".tmp"
+        _run([nvcc, "-shared", "-o", tmp] + ARCH + objs + [obj, "-cudart", "static"], verbose)
+        os.replace(tmp, TIMEOUT_VARIANT_LIB)
+    return TIMEOUT_VARIANT_LIB
 
 
 if __name__ == "__main__":

@@ -60,7 +60,15 @@ __device__ __forceinline__ float round_p_exact(float p, int mode) {
 }
 
 // ------------------------------------------------------------ sync helpers
-constexpr uint32_t kExactSpin = 1u << 22;         // bounded waits (then the row is NaN)
+// Bounded waits: after this many polls a hand-off wait gives up, the row is
+// NaN and KATTN_DEVERR_TIMEOUT is set.  The library is built with the default;
+// a test-only build of this file (build.py, build_exact_timeout_variant) sets
+// it to 0 so that every wait runs out at once and the give-up path is
+// exercised without any wait that could block.
+#ifndef KATTN_EXACT_SPIN_LIMIT
+#define KATTN_EXACT_SPIN_LIMIT (1u << 22)
+#endif
+constexpr uint32_t kExactSpin = KATTN_EXACT_SPIN_LIMIT;
 
 __device__ __forceinline__ void ex_mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
@@ -130,6 +138,7 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
 
   if (!sequence_valid(p, b)) {
     if (!producer) orow[gt] = __int_as_float(0x7fc00000);
+    if (tid == 0 && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_BAD_SEQUENCE);
     return;
   }
   const int L = p.ctx_len[b] + j;
@@ -204,9 +213,12 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
       // The chains must be done with chunk c - 2: its K/V stage takes chunk
       // c + 1 now, and its tok buffer takes chunk c.
       if (c >= 2) {
-        if (gt == 0) sm.ok_p = ex_mbar_wait(&sm.empty[tb], ((c - 2) >> 1) & 1);
+        if (gt == 0) {
+          sm.ok_p = ex_mbar_wait(&sm.empty[tb], ((c - 2) >> 1) & 1);
+          if (!sm.ok_p && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
+        }
         group_sync(1);
-        if (!sm.ok_p) break;
+        if (!sm.ok_p) break;                      // the copies in flight drain below
       }
       if (c + 1 < nchunks) {
         stage_rows(t0 + kChunk, (c + 1) % kStages);
@@ -272,7 +284,10 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   bool ok = true;
   for (int c = 0; c < nchunks; ++c) {
     const int st = c % kStages, tb = c & 1, n = min(kChunk, L - c * kChunk);
-    if (gt == 0) sm.ok_c = ex_mbar_wait(&sm.full[tb], (c >> 1) & 1);
+    if (gt == 0) {
+      sm.ok_c = ex_mbar_wait(&sm.full[tb], (c >> 1) & 1);
+      if (!sm.ok_c && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
+    }
     group_sync(2);
     if (!sm.ok_c) {
       ok = false;

@@ -25,7 +25,7 @@
 // the window's end each warp merges the four spans for its 32 channels in the
 // same order as the M = 1 kernel.  PG: the paged cache, block rows from the
 // block table.
-#include "decode_split.cuh"
+#include "tcgen05_common.cuh"
 
 namespace kattn {
 namespace {
@@ -35,8 +35,7 @@ constexpr int kTcWarps = 4;
 constexpr int kTcStages = 4;                     // TMA stages of 32 keys (K and V)
 constexpr int kTcCols = kSpansPerCta * kTcRows;  // tensor-memory columns: 128
 constexpr int kTcCtasPerSm = 512 / kTcCols;       // resident CTAs: all of tensor memory
-// kind::f16 with f32 accumulate, A and B f16 and K-major, N = 32, M = 128
-constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcRows >> 3) << 17) | ((128u >> 4) << 24);
+static_assert(kTcRows == kTcN, "the instruction descriptor's N");
 
 struct __align__(1024) TcSmem {
   uint8_t ring[kTcStages][2][kBlockBytes];       // K and V blocks of 32 keys (128-byte swizzle)
@@ -56,110 +55,6 @@ struct __align__(1024) TcSmem {
   // block n + 1 before a slower one has read the flag of block n.
   int fail[2];
 };
-
-__device__ __forceinline__ int op_off(int row, int key) {   // bytes, see TcSmem
-  return (row >> 3) * 256 + (key >> 3) * 128 + (row & 7) * 16 + (key & 7) * 2;
-}
-
-__device__ __forceinline__ uint64_t smem_desc(const void* p) {
-  uint64_t d = (uint64_t)((smem_u32(p) >> 4) & 0x3FFFu);
-  d |= (uint64_t)(128u >> 4) << 16;              // K-direction core-matrix stride
-  d |= (uint64_t)(256u >> 4) << 32;              // 8-row group stride
-  d |= (uint64_t)1 << 46;                        // descriptor version
-  return d;                                      // layout: no swizzle
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, 1, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(kTcIdesc));
-}
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
-               ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-// 16 consecutive columns of the calling warp's 32 lanes: load (waits), and
-// store (no wait: tc_wait_st before the data is used by another thread).
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16};\n"
-      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
-      "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
-      "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
-      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
-      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
-      : "memory");
-}
-__device__ __forceinline__ void tc_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-}
-// 8 consecutive columns of the calling warp's 32 lanes.
-__device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-// Store 32 consecutive columns of the calling warp's 32 lanes (waits for the store).
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
-      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
-      "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
-      "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
-      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
-      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
-      "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
-      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
-      "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
-      "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
-      "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-}
-
-// Paged layout: the block-table entry of key `key` of sequence b, and the
-// cache row it gives (paged_row in two steps, so that the table load can be
-// issued an item ahead of its use).  An entry outside the pool flags
-// KATTN_DEVERR_BAD_PAGE and reads page 0.
-__device__ __forceinline__ int tc_page_entry(const DecodeParams& p, int b, int key) {
-  return __ldg(p.block_table + (int64_t)b * p.max_pages + (key >> p.page_shift));
-}
-__device__ __forceinline__ int tc_page_row(const DecodeParams& p, int page, int key) {
-  if ((unsigned)page >= (unsigned)p.n_pages) {
-    if (p.err_word) atomicOr(p.err_word, KATTN_DEVERR_BAD_PAGE);
-    page = 0;
-  }
-  return (page << p.page_shift) | (key & ((1 << p.page_shift) - 1));
-}
 
 template <int PM, bool PG>
 __global__ void __launch_bounds__(kTcWarps * 32, kTcCtasPerSm)

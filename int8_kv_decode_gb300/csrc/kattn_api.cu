@@ -87,6 +87,11 @@ int run_decode(DecodeParams& p, int p_mode, int exact_mode, float sm_scale, cons
   if (!aligned(v, 16) || !aligned(v_scale, 4) || !aligned(out, 16)) return KATTN_ERR_MISALIGNED;
   cudaError_t e;
   if (exact_mode) {
+    // no workspace needed; one that is given receives the device error bits
+    if (workspace != nullptr) {
+      if (!aligned(workspace, 256) || workspace_bytes < 256) return KATTN_ERR_WORKSPACE;
+      p.err_word = static_cast<uint32_t*>(workspace);
+    }
     e = launch_decode_exact(p, expf_constants(), as_stream(stream));
   } else {
     const WorkspaceLayout w = workspace_layout(p.B, p.M, p.Hq, p.max_ctx);

@@ -251,6 +251,22 @@ def test_window_constant_matches_header():
     assert int(re.search(r"#define KATTN_WINDOW_KEYS (\d+)", text).group(1)) == api.WINDOW_KEYS
 
 
+def test_device_error_bits_match_header():
+    from int8_kv_decode_gb300 import api
+    text = open(HEADER, encoding="utf-8").read()
+    for name in ("BAD_SEQUENCE", "TIMEOUT", "BAD_PAGE"):
+        val = int(re.search(rf"#define KATTN_DEVERR_{name} (0x[0-9a-f]+)u", text).group(1), 16)
+        assert getattr(api, f"DEVERR_{name}") == val, name
+
+
+def test_exact_mode_workspace_validation(lib):
+    # exact mode: the workspace is optional, but one that is given must hold
+    # the 256-byte error word and be 256-byte aligned
+    WS = -4
+    assert _decode(lib, exact=1, ws=0x1010, ws_bytes=256) == WS
+    assert _decode(lib, exact=1, ws=0x1100, ws_bytes=128) == WS
+
+
 def test_launch_count_validation(lib):
     f = lib.kattn_decode_launch_count
     assert f(0, 1, 32, 4, 1024) == 0          # no sequences
