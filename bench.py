@@ -46,8 +46,6 @@ KERNEL_SOURCES = {
     "decode_fast_kernel": ["decode_fast.cu", "decode_split.cuh"] + _COMMON_SOURCES,
     "decode_tc_kernel": ["decode_fast.cu", "decode_split.cuh", "tcgen05_common.cuh",
                          "decode_tc.cu"] + _COMMON_SOURCES,
-    "decode_tcw_kernel": ["decode_fast.cu", "decode_split.cuh", "tcgen05_common.cuh",
-                          "decode_tcw.cu"] + _COMMON_SOURCES,
     "decode_exact_kernel": ["decode_exact.cu"] + _COMMON_SOURCES,
 }
 

@@ -33,7 +33,6 @@ SOURCES = {
     "decode_fast.cu": [],
     "decode_fast_paged.cu": [],
     "decode_tc.cu": [],
-    "decode_tcw.cu": [],
     "decode_noalloc.cu": [],
     "decode_exact.cu": ["--fmad=false"],
     "expf_constants.cu": ["--fmad=false"],

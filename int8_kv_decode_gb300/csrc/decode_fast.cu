@@ -342,7 +342,7 @@ cudaError_t launch_split_contiguous(const DecodeParams& p, const TmaMaps& maps,
     return launch_modes<1, 1, false>(pr, maps, stream);
   }
   if (p.R <= 16) return launch_modes<2, 1, false>(p, maps, stream);
-  if (p.R <= 32) return launch_split_17_32(p, maps, stream);   // P.V on tcgen05
+  if (p.R <= 32) return launch_split_tc(p, maps, stream);   // P.V on tcgen05
   if (p.R <= 48) return launch_modes<3, 2, false>(p, maps, stream);
   return launch_modes<4, 2, false>(p, maps, stream);
 }

@@ -13,7 +13,7 @@ cudaError_t launch_split_paged(const DecodeParams& p, const TmaMaps& maps, cudaS
     return launch_modes<1, 1, true>(pr, maps, stream);
   }
   if (p.R <= 16) return launch_modes<2, 1, true>(p, maps, stream);
-  if (p.R <= 32) return launch_split_17_32(p, maps, stream);   // P.V on tcgen05 (decode_tc.cu)
+  if (p.R <= 32) return launch_split_tc(p, maps, stream);   // P.V on tcgen05 (decode_tc.cu)
   if (p.R <= 48) return launch_modes<3, 2, true>(p, maps, stream);
   return launch_modes<4, 2, true>(p, maps, stream);
 }

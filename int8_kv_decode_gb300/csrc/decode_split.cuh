@@ -1053,15 +1053,4 @@ cudaError_t launch_split_paged(const DecodeParams& p, const TmaMaps& maps, cudaS
 // the fifth-generation tensor cores (decode_tc.cu), contiguous or paged cache.
 cudaError_t launch_split_tc(const DecodeParams& p, const TmaMaps& maps, cudaStream_t stream);
 
-// The same rows with warps that own spans (decode_tcw.cu): 8 warps, each
-// reducing one span for 16 of the rows.
-cudaError_t launch_split_tcw(const DecodeParams& p, const TmaMaps& maps, cudaStream_t stream);
-
-// Which of the two tcgen05 kernels serves 17..32 rows.
-constexpr bool kSpanWarpsTc = true;
-inline cudaError_t launch_split_17_32(const DecodeParams& p, const TmaMaps& maps,
-                                      cudaStream_t stream) {
-  return kSpanWarpsTc ? launch_split_tcw(p, maps, stream) : launch_split_tc(p, maps, stream);
-}
-
 }  // namespace kattn
