@@ -19,7 +19,7 @@ namespace kattn {
 namespace {
 
 constexpr int kChunk = 128;
-constexpr int kSub = 16;                          // keys per step of the serial scan
+constexpr int kSub = 32;                          // keys per step of the serial scan
 
 // f32 of a signed byte, exactly: the offset-binary byte u = v + 128 placed in
 // the low mantissa bits of 1.5 * 2^23 gives 12582912 + u; subtracting
@@ -293,54 +293,34 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
       ok = false;
       break;
     }
-    // kSub keys at a time: the chain steps of keys u0 .. u0 + kSub - 1, each
-    // with its term round_p(p) * (f32(v8) * vs) computed one sub-block
-    // earlier, interleaved with the terms of the next kSub keys (independent
-    // of the chains, so they fill the chains' latency).  Terms of keys past n
-    // read stale but in-bounds entries of the stage and are never used.
+    // 32 keys at a time: first every key's term round_p(p) * (f32(v8) * vs)
+    // (independent of one another), then the two chains, key by key.
     const uint8_t* vcol = reinterpret_cast<const uint8_t*>(&sm.v[st][0][gt]);
     const float2* tk2 = reinterpret_cast<const float2*>(sm.tok[tb]);
-    auto term_of = [&](int u) {
-      const float2 pv = tk2[2 * u];               // round_p(p), v_scale
-      return __fmul_rn(pv.x, __fmul_rn(i8_to_f32(vcol[u * kD]), pv.y));
-    };
-    float tcur[kSub];
-#pragma unroll
-    for (int i = 0; i < kSub; ++i) tcur[i] = term_of(i);
     for (int u0 = 0; u0 < n; u0 += kSub) {
-      const int u1 = u0 + kSub;
-      float tnext[kSub];
-      if (u1 <= n) {
-        if (u1 < kChunk) {
+      float term[kSub];
 #pragma unroll
-          for (int i = 0; i < kSub; ++i) {
-            const float2 ap = tk2[2 * (u0 + i) + 1];   // alpha, p
-            o = __fadd_rn(__fmul_rn(o, ap.x), tcur[i]);
-            l = __fadd_rn(__fmul_rn(l, ap.x), ap.y);
-            tnext[i] = term_of(u1 + i);
-          }
-        } else {
+      for (int i = 0; i < kSub; ++i) {
+        const float2 pv = tk2[2 * (u0 + i)];      // round_p(p), v_scale
+        term[i] = __fmul_rn(pv.x, __fmul_rn(i8_to_f32(vcol[(u0 + i) * kD]), pv.y));
+      }
+      if (u0 + kSub <= n) {
 #pragma unroll
-          for (int i = 0; i < kSub; ++i) {
-            const float2 ap = tk2[2 * (u0 + i) + 1];
-            o = __fadd_rn(__fmul_rn(o, ap.x), tcur[i]);
-            l = __fadd_rn(__fmul_rn(l, ap.x), ap.y);
-            tnext[i] = 0.0f;                      // the chunk ends here
-          }
+        for (int i = 0; i < kSub; ++i) {
+          const float2 ap = tk2[2 * (u0 + i) + 1];   // alpha, p
+          o = __fadd_rn(__fmul_rn(o, ap.x), term[i]);
+          l = __fadd_rn(__fmul_rn(l, ap.x), ap.y);
         }
       } else {
 #pragma unroll
         for (int i = 0; i < kSub; ++i) {
-          tnext[i] = 0.0f;                        // the row ends in this sub-block
           if (u0 + i < n) {
             const float2 ap = tk2[2 * (u0 + i) + 1];
-            o = __fadd_rn(__fmul_rn(o, ap.x), tcur[i]);
+            o = __fadd_rn(__fmul_rn(o, ap.x), term[i]);
             l = __fadd_rn(__fmul_rn(l, ap.x), ap.y);
           }
         }
       }
-#pragma unroll
-      for (int i = 0; i < kSub; ++i) tcur[i] = tnext[i];
     }
     group_sync(2);                                // every chain is done with chunk c
     if (gt == 0) ex_mbar_arrive(&sm.empty[tb]);
