@@ -450,26 +450,39 @@ def run_ours(args):
         step(i)
     torch.cuda.synchronize(dev)
 
-    # One CUDA graph per cache copy for the step and for the decode alone:
-    # a replay is one host call, so small steps are timed on the GPU rather
-    # than on the Python launch path.  The graphs hold the same launches as
-    # the eager calls above (the warm-up already did the one-time set-up).
-    run_step, run_decode = step, decode
+    # CUDA graphs per cache copy for the step and for the decode alone: one
+    # graph holds a single step, another G consecutive steps on consecutive
+    # cache copies (as a model step's graph holds a layer's attention call
+    # between its other kernels, so the graph's own launch is not paid per
+    # call).  A replay is one host call, so small steps are timed on the GPU
+    # rather than on the Python launch path.  The graphs hold the same
+    # launches as the eager calls above (the warm-up did the one-time set-up).
+    G = max(1, int(args.graph_steps))
+    run_steps = lambda i0, n: [step(i0 + k) for k in range(n)]       # noqa: E731
+    run_decodes = lambda i0, n: [decode(i0 + k) for k in range(n)]   # noqa: E731
     if not args.no_graphs:
-        g_step, g_dec = [], []
+        graphs = {}
         for c in range(n_copies):
-            gs, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gs, capture_error_mode="thread_local"):
-                step(c)
-            with torch.cuda.graph(gd, capture_error_mode="thread_local"):
-                decode(c)
-            g_step.append(gs)
-            g_dec.append(gd)
-        run_step = lambda i: g_step[i % n_copies].replay()     # noqa: E731
-        run_decode = lambda i: g_dec[i % n_copies].replay()    # noqa: E731
+            for n in sorted({1, G}):
+                gs, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gs, capture_error_mode="thread_local"):
+                    run_steps(c, n)
+                with torch.cuda.graph(gd, capture_error_mode="thread_local"):
+                    run_decodes(c, n)
+                graphs[(c, n)] = (gs, gd)
+        run_steps = lambda i0, n: graphs[(i0 % n_copies, n)][0].replay()     # noqa: E731
+        run_decodes = lambda i0, n: graphs[(i0 % n_copies, n)][1].replay()   # noqa: E731
         for i in range(args.warmup):
-            run_step(i)
+            run_steps(i, 1)
         torch.cuda.synchronize(dev)
+
+    def timed(run, i0, k):
+        """Exactly k steps from step index i0: graphs of G steps, then single ones."""
+        i = 0
+        while i < k:
+            n = G if k - i >= G else 1
+            run(i0 + i, n)
+            i += n
     stream = torch.cuda.current_stream(dev)
     if pg is not None:
         dist.barrier()
@@ -492,8 +505,7 @@ def run_ours(args):
         dist.barrier()
     wall0 = time.time()
     start.record(stream)
-    for i in range(args.steps):
-        run_step(args.warmup + i)
+    timed(run_steps, args.warmup, args.steps)
     end.record(stream)
     torch.cuda.synchronize(dev)
     if pg is not None:
@@ -505,8 +517,7 @@ def run_ours(args):
     d_start, d_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     d_start.record(stream)
-    for i in range(args.steps):
-        run_decode(args.warmup + i)
+    timed(run_decodes, args.warmup, args.steps)
     d_end.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -588,7 +599,10 @@ def run_ours(args):
         "config": workload_config(
             wl, x.ctx, l2=(f"inputs larger than L2: {kvb / 1e9:.2f} GB KV per step x "
                            f"{n_copies} rotating cache copies vs {l2 / 2**20:.0f} MiB L2"),
-            launch="eager" if args.no_graphs else "one CUDA graph replay per step",
+            launch=("eager" if args.no_graphs else
+                    "one CUDA graph replay per step" if G == 1 else
+                    f"CUDA graphs of {G} consecutive steps on consecutive cache copies "
+                    f"(a remainder of single-step graphs), {args.steps} steps timed"),
             p_mode=args.p_mode, exact=exact, page_rows=P),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
@@ -633,6 +647,8 @@ def main(argv=None):
                          "order (default: the contiguous cache)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every step eagerly instead of replaying CUDA graphs")
+    ap.add_argument("--graph-steps", type=int, default=8,
+                    help="steps captured in one CUDA graph (1: one graph replay per step)")
     ap.add_argument("--ref-sequences", type=int, default=2,
                     help="sequences per step of the reference arm")
     args = ap.parse_args(argv)

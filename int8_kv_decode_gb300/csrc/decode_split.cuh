@@ -202,6 +202,17 @@ __device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
   return f2_unpack(r);
 }
 
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(r);
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
+  return f2_unpack(r);
+}
+
 // x = hi + lo with hi = RN_f16(x) and lo = RN_f16(x - hi) (x - hi is exact in
 // float32): 22 significant bits of each of two values, packed as f16x2.
 __device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -243,6 +254,66 @@ __device__ __forceinline__ float round_p_t(float p) {
   } else {
     return p;
   }
+}
+
+// Online-softmax update of one 8-row n-tile over a 32-key block, for the two
+// rows 2c, 2c + 1 a thread holds (e = 0, 1).  s0 / s1: the scores of the block's
+// two 16-key halves in the MMA score layout ([0] key g row 2c, [1] key g row
+// 2c+1, [2] key g+8 row 2c, [3] key g+8 row 2c+1); on return they hold the
+// P.V operand values a = round_p(p) * v_scale * 2^E.  vs4[q]: v_scale of key
+// g + 8q.  The two rows go through paired float32 operations, each element
+// rounded as the scalar operation would be:
+//   m' = max(m, block max);  alpha = e^(m - m');  p = e^(s - m')
+//   l  = l * alpha + ((p_g + p_g8) + (p_16+g + p_24+g))   (one fused multiply-add)
+// A row with no visible key yet (m' = -inf) is left untouched (alpha 1, p 0).
+template <int PM>
+__device__ __forceinline__ void softmax_tile(float (&s0)[4], float (&s1)[4], float (&m_run)[2],
+                                             float (&l_run)[2], const float (&up)[2],
+                                             const float (&vs4)[4], float (&alpha)[2],
+                                             bool& rescale) {
+  float mnew[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float bm = fmaxf(fmaxf(s0[e], s0[2 + e]), fmaxf(s1[e], s1[2 + e]));
+    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+    mnew[e] = fmaxf(m_run[e], bm);
+  }
+  const float2 mn = make_float2(mnew[0], mnew[1]);
+  const float2 l2e = make_float2(kLog2e, kLog2e);
+  const bool live0 = mnew[0] != -INFINITY, live1 = mnew[1] != -INFINITY;
+  const float2 da = f2_mul(f2_sub(make_float2(m_run[0], m_run[1]), mn), l2e);
+  alpha[0] = live0 ? fast_exp2(da.x) : 1.0f;
+  alpha[1] = live1 ? fast_exp2(da.y) : 1.0f;
+  rescale |= (alpha[0] != 1.0f) | (alpha[1] != 1.0f);
+  m_run[0] = mnew[0];
+  m_run[1] = mnew[1];
+  float2 pk[2][2];                                // [half][key g | g + 8], rows (2c, 2c+1)
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float* sv = hf ? s1 : s0;
+      const float2 d = f2_mul(f2_sub(make_float2(sv[2 * k], sv[2 * k + 1]), mn), l2e);
+      pk[hf][k] = make_float2(live0 ? fast_exp2(d.x) : 0.0f, live1 ? fast_exp2(d.y) : 0.0f);
+    }
+  const float2 lsum = f2_add(f2_add(pk[0][0], pk[0][1]), f2_add(pk[1][0], pk[1][1]));
+  const float2 lnew = f2_fma(make_float2(l_run[0], l_run[1]), make_float2(alpha[0], alpha[1]), lsum);
+  l_run[0] = lnew.x;
+  l_run[1] = lnew.y;
+  const float2 up2 = make_float2(up[0], up[1]);
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float v = vs4[2 * hf + k];
+      const float2 a = f2_mul(f2_mul(make_float2(round_p_t<PM>(pk[hf][k].x), round_p_t<PM>(pk[hf][k].y)),
+                                     make_float2(v, v)), up2);
+      float* sv = hf ? s1 : s0;
+      sv[2 * k] = a.x;
+      sv[2 * k + 1] = a.y;
+    }
 }
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a block written by TMA
@@ -699,40 +770,14 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
             }
       }
 
-      // ---- online softmax update of rows 8nr + 2c + e over the 32-key block
+      // ---- online softmax update of rows 8nr + 2c + e over the 32-key block;
+      // a = round_p(p) * v_scale is kept in the score layout (sc is done with)
       float alpha[NR][2];
       bool rescale = false;
 #pragma unroll
       for (int nr = 0; nr < NR; ++nr)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float bm = fmaxf(fmaxf(sc[0][nr][e], sc[0][nr][2 + e]), fmaxf(sc[1][nr][e], sc[1][nr][2 + e]));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-          const float mnew = fmaxf(m_run[nr][e], bm);
-          float a = 1.0f, pk[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
-          if (mnew != -INFINITY) {                  // else: no visible key yet, row untouched
-            a = exp_diff(m_run[nr][e], mnew);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              pk[hf][0] = exp_diff(sc[hf][nr][e], mnew);
-              pk[hf][1] = exp_diff(sc[hf][nr][2 + e], mnew);
-            }
-          }
-          alpha[nr][e] = a;
-          rescale |= (a != 1.0f);
-          m_run[nr][e] = mnew;
-          l_run[nr][e] = __fmaf_rn(l_run[nr][e], a,
-                                   __fadd_rn(__fadd_rn(pk[0][0], pk[0][1]), __fadd_rn(pk[1][0], pk[1][1])));
-          // a = round_p(p) * v_scale, kept in the score layout (sc is done with)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            sc[hf][nr][e] = __fmul_rn(__fmul_rn(round_p_t<PM>(pk[hf][0]), vs4[2 * hf]), up_row[nr][e]);
-            sc[hf][nr][2 + e] =
-                __fmul_rn(__fmul_rn(round_p_t<PM>(pk[hf][1]), vs4[2 * hf + 1]), up_row[nr][e]);
-          }
-        }
+        softmax_tile<PM>(sc[0][nr], sc[1][nr], m_run[nr], l_run[nr], up_row[nr], vs4, alpha[nr],
+                         rescale);
       if (rescale) {
 #pragma unroll
         for (int md = 0; md < 8; ++md)

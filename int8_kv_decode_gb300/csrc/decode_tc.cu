@@ -302,36 +302,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
               if (key >= Lrow[u & 1]) sc[hf][u] = -INFINITY;
             }
         }
-        // ---- online softmax of rows row0 + 2c + e over the block
+        // ---- online softmax of rows row0 + 2c + e over the block (a in sc)
         float alpha[2];
         bool rescale = false;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float bm = fmaxf(fmaxf(sc[0][e], sc[0][2 + e]), fmaxf(sc[1][e], sc[1][2 + e]));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
-          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
-          const float mnew = fmaxf(m_run[e], bm);
-          float a = 1.0f, pk[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
-          if (mnew != -INFINITY) {
-            a = exp_diff(m_run[e], mnew);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              pk[hf][0] = exp_diff(sc[hf][e], mnew);
-              pk[hf][1] = exp_diff(sc[hf][2 + e], mnew);
-            }
-          }
-          alpha[e] = a;
-          rescale |= (a != 1.0f);
-          m_run[e] = mnew;
-          l_run[e] = __fmaf_rn(l_run[e], a,
-                               __fadd_rn(__fadd_rn(pk[0][0], pk[0][1]), __fadd_rn(pk[1][0], pk[1][1])));
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            sc[hf][e] = __fmul_rn(__fmul_rn(round_p_t<PM>(pk[hf][0]), vs4[2 * hf]), up_row[e]);
-            sc[hf][2 + e] = __fmul_rn(__fmul_rn(round_p_t<PM>(pk[hf][1]), vs4[2 * hf + 1]), up_row[e]);
-          }
-        }
+        softmax_tile<PM>(sc[0], sc[1], m_run, l_run, up_row, vs4, alpha, rescale);
         // ---- P operand words: {a[key 2c][row g], a[key 2c+1][row g]} and keys
         // 2c+8, 2c+9 of each half, split into f16 hi + lo (as the M = 1 kernel's
         // B fragments)
