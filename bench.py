@@ -81,12 +81,23 @@ def load_peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def roofline_kernel(g: int, M: int, exact: bool) -> str:
-    """The decode kernel a call launches: exact mode, P.V on tcgen05 for
-    17..32 query rows per (sequence, kv head), else the mma.sync split pass."""
+ROW_GROUP_MAX_ITEMS = 4096   # the library's bound on work items for row groups
+WINDOW_KEYS = 512
+
+
+def roofline_kernel(g: int, M: int, exact: bool, B: int = 1 << 20, max_ctx: int = 1 << 20,
+                    Hkv: int = 1) -> str:
+    """The decode kernel a call launches: exact mode; the one-tile mma.sync
+    kernel for up to 8 query rows per (sequence, kv head), and for more rows
+    when the batch has few work items (row groups); P.V on tcgen05 for 17..32
+    rows; else the mma.sync split pass."""
     if exact:
         return "decode_exact_kernel"
-    return "decode_tc_kernel" if 16 < g * M <= 32 else "decode_fast_kernel"
+    R = g * M
+    items = B * ((max_ctx + M - 1 + WINDOW_KEYS - 1) // WINDOW_KEYS) * Hkv   # an upper bound
+    if R > 8 and items <= ROW_GROUP_MAX_ITEMS:
+        return "decode_fast_kernel"
+    return "decode_tc_kernel" if 16 < R <= 32 else "decode_fast_kernel"
 
 
 def kernel_source_sha(kernel: str = "decode_fast_kernel", paged: bool = False) -> str:
@@ -561,7 +572,7 @@ def run_ours(args):
     peak, peak_kind = load_peak_hbm()
     algo = kvb + qob
     achieved = algo / decode_s / 1e9
-    rkernel = roofline_kernel(wl.Hq // wl.Hkv, wl.M, exact)
+    rkernel = roofline_kernel(wl.Hq // wl.Hkv, wl.M, exact, B, max_ctx, Hkv)
     sha = kernel_source_sha(rkernel, paged=bool(P) and not exact)
     clocks = None
     try:

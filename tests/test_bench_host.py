@@ -102,6 +102,10 @@ def test_roofline_kernel_follows_the_dispatch():
     assert bench.roofline_kernel(8, 4, False) == "decode_tc_kernel"        # R = 32
     assert bench.roofline_kernel(8, 5, False) == "decode_fast_kernel"      # R = 40
     assert bench.roofline_kernel(8, 4, True) == "decode_exact_kernel"
+    # few work items: more than 8 rows go to row groups of the one-tile kernel
+    assert bench.roofline_kernel(8, 4, False, 6, 3000, 2) == "decode_fast_kernel"
+    assert bench.roofline_kernel(8, 4, False, 64, 32768, 4) == "decode_tc_kernel"
+    assert bench.roofline_kernel(8, 1, False, 6, 3000, 2) == "decode_fast_kernel"
 
 
 def test_paged_rows_and_traffic_key():
