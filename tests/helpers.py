@@ -70,6 +70,24 @@ def upload(wl, rep=0, ctx_override=None, device="cuda"):
                    ctx=torch.from_numpy(x.ctx).to(dev), ok8=ok8, oks=oks, ov8=ov8, ovs=ovs)
 
 
+def device_upload(wl, rep=0):
+    """A workload drawn and quantized on the GPU (large shapes), as a GpuCase
+    without the oracle's caches (ok8 .. ovs are None)."""
+    import torch
+    import int8_kv_decode_gb300 as K
+    x = make_workload(wl, rep=rep, device="cuda")
+    k8 = torch.empty((wl.Hkv, x.cap_rows, wl.d), dtype=torch.int8, device="cuda")
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((wl.Hkv, x.cap_rows), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    K.quantize_kv(x.k_rows, k8, ks)
+    K.quantize_kv(x.v_rows, v8, vs)
+    x.k_rows = x.v_rows = None
+    return GpuCase(x=x, k8=k8, v8=v8, ks=ks, vs=vs, q=x.q,
+                   rs=torch.from_numpy(x.row_start).cuda(), ctx=torch.from_numpy(x.ctx).cuda(),
+                   ok8=None, oks=None, ov8=None, ovs=None)
+
+
 def run(c: GpuCase, **kw):
     import int8_kv_decode_gb300 as K
     return K.decode(c.q, c.k8, c.ks, c.v8, c.vs, c.rs, c.ctx, c.x.max_ctx, **kw)

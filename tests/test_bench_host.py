@@ -95,7 +95,8 @@ def test_all_cores_oracle_baseline_runs_in_spawned_processes():
 
 
 def test_roofline_kernel_follows_the_dispatch():
-    # 17..32 query rows per (sequence, kv head) run the tcgen05 P.V kernel.
+    # 17..32 query rows per (sequence, kv head) with many work items run the
+    # tcgen05 P.V kernel; with few, row groups of the one-tile kernel.
     assert bench.roofline_kernel(8, 1, False) == "decode_fast_kernel"
     assert bench.roofline_kernel(8, 2, False) == "decode_fast_kernel"      # R = 16
     assert bench.roofline_kernel(8, 3, False) == "decode_tc_kernel"        # R = 24

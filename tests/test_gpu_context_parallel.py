@@ -93,8 +93,9 @@ def test_spec_verify_shards_equal_single_gpu_bytes(n_shards, p_mode):
 
 @pytest.mark.parametrize("n_shards", [2, 3])
 def test_r32_shards_equal_single_gpu_bytes(n_shards):
-    # 32 query rows per kv head (M = 4, GQA 8): the tcgen05 kernel's window
-    # partials in shard mode, gathered and merged, give the single-GPU bytes.
+    # 32 query rows per kv head (M = 4, GQA 8; 8 sequences: row groups): the
+    # window partials in shard mode, gathered and merged, give the single-GPU
+    # bytes.
     import int8_kv_decode_gb300 as K
     wl = custom("cp_r32", 8, 4, 16, 2, ("uniform", 300, 5000), outliers=True)
     c = upload(wl)

@@ -228,3 +228,39 @@ def test_quantize_kv_rows_against_the_oracle():
     want_s[:, dst[keep]] = nks[:, keep]
     assert np.array_equal(q8.cpu().numpy(), want_q)
     assert np.array_equal(bits(sc.cpu().numpy()), bits(want_s))
+
+
+@pytest.mark.parametrize("g,M", [(8, 3), (4, 5)])
+def test_tcgen05_kernel_at_24_and_20_rows(g, M):
+    # 17..32 query rows per kv head with more work items than the row-group
+    # bound (48 sequences x about 50 windows x 2 kv heads > 4096): the tcgen05
+    # kernel.  Every draft column equals the M = 1 decode byte for byte, and
+    # sampled rows meet the oracle.
+    import torch
+    import int8_kv_decode_gb300 as K
+    wl = custom(f"tc_r{g * M}", 48, M, 2 * g, 2, ("uniform", 20000, 30000), outliers=True,
+                index=31)
+    x = make_workload(wl, device="cuda")
+    windows = (int(x.ctx.max()) + M - 1 + 511) // 512
+    assert wl.B * windows * wl.Hkv > 4096
+    k8 = torch.empty((wl.Hkv, x.cap_rows, wl.d), dtype=torch.int8, device="cuda")
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((wl.Hkv, x.cap_rows), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    K.quantize_kv(x.k_rows, k8, ks)
+    K.quantize_kv(x.v_rows, v8, vs)
+    rs = torch.from_numpy(x.row_start).cuda()
+    ctx = torch.from_numpy(x.ctx).cuda()
+    out = K.decode(x.q, k8, ks, v8, vs, rs, ctx, x.max_ctx).cpu().numpy()
+    for j in range(M):
+        one = K.decode(x.q[:, j:j + 1].contiguous(), k8, ks, v8, vs, rs, ctx + j,
+                       x.max_ctx + j).cpu().numpy()
+        assert np.array_equal(bits(out[:, j:j + 1]), bits(one)), j
+    got, ref = [], []
+    for b in (0, int(np.argmax(x.ctx)), wl.B - 1):
+        rr = [(j, (j + kh) % g + kh * g) for j in range(M) for kh in range(wl.Hkv)]
+        o = oracle_sequence_rows(x, b, oracle_sequence_cache(x, b, k8, ks, v8, vs), rr)
+        for (j, h) in rr:
+            got.append(out[b, j, h])
+            ref.append(o[j, h])
+    _compare(np.array(got), np.array(ref), 0)

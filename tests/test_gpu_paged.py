@@ -11,7 +11,7 @@ unused table entries are -1, so a read of anything else shows up.
 import numpy as np
 import pytest
 
-from helpers import custom, oracle_decode, run, upload
+from helpers import custom, device_upload, oracle_decode, run, upload
 from synth import WORKLOADS, make_workload
 from synth.paging import page_layout, paged_copy
 
@@ -96,12 +96,16 @@ def test_paged_full_size_serving_m4_equals_contiguous():
     assert K.get_device_status(ws) == 0
 
 
-@pytest.mark.parametrize("M,Hq", [(2, 8), (4, 16)])    # R = 8 (mma.sync) and R = 32 (tcgen05)
-def test_paged_bad_tables_are_flagged_without_touching_other_sequences(M, Hq):
+# R = 8: the one-tile kernel; R = 32 with 6 sequences: its row groups; R = 32
+# with 48 long sequences (more work items than the row-group bound): tcgen05
+@pytest.mark.parametrize("M,Hq,B,ctx", [(2, 8, 6, ("uniform", 100, 900)),
+                                        (4, 16, 6, ("uniform", 100, 900)),
+                                        (4, 16, 48, ("uniform", 20000, 30000))])
+def test_paged_bad_tables_are_flagged_without_touching_other_sequences(M, Hq, B, ctx):
     import torch
     import int8_kv_decode_gb300 as K
-    wl = custom(f"paged_bad_m{M}", 6, M, Hq, 2, ("uniform", 100, 900), outliers=False)
-    c = upload(wl)
+    wl = custom(f"paged_bad_m{M}_b{B}", B, M, Hq, 2, ctx, outliers=False)
+    c = upload(wl) if B <= 8 else device_upload(wl)
     pc = Paged(c, 64, seed=3)
     ws = K.alloc_workspace(wl.B, wl.M, wl.Hq, c.x.max_ctx)
     clean = pc.decode(c, workspace=ws).cpu().numpy()

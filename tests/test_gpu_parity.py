@@ -243,7 +243,7 @@ def test_many_short_sequences(B, M, Hq):
         assert np.array_equal(bits(got[lo:hi]), bits(half)), (lo, hi)
 
 
-@pytest.mark.parametrize("shape", ["spec_verify", "r32"])   # mma.sync (R = 40), tcgen05 (R = 32)
+@pytest.mark.parametrize("shape", ["spec_verify", "r32"])   # row groups at R = 40 and R = 32
 def test_decode_replays_in_a_cuda_graph(shape):
     # The three launches of a fast decode, captured once and replayed, give
     # the bytes of an ordinary call.
@@ -301,7 +301,7 @@ def test_decode_append_equals_separate_calls(name, p_mode):
     # as kattn_quantize_kv_rows twice followed by kattn_decode.
     import torch
     import int8_kv_decode_gb300 as K
-    # r32: 32 query rows per kv head (M = 4, GQA 8), the tcgen05 kernel
+    # r32: 32 query rows per kv head (M = 4, GQA 8) over 6 sequences: row groups
     wl = WORKLOADS[name] if name != "r32" else custom("append_r32", 6, 4, 16, 2,
                                                        ("uniform", 200, 3000), outliers=True)
     x = make_workload(wl, rep=5)
@@ -385,7 +385,7 @@ def test_long_rows_alone_equal_the_batch(p_mode):
 
 def test_e4m3_direct_mode_columns_and_oracle():
     # p_mode 5 (e4m3 P into the tensor-core P.V, one f16 operand): the M = 4
-    # batch (32 rows per kv head: the tcgen05 kernel) against the oracle with
+    # batch (32 rows per kv head over 5 sequences: row groups) against the oracle with
     # the same rounding, every draft column equal to the M = 1 decode (the
     # mma.sync kernel) byte for byte, and no exact-mode form.
     import int8_kv_decode_gb300 as K

@@ -36,7 +36,7 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(name):
     import torch
     import __graft_entry__
     __graft_entry__.build()
-    # r32: 32 query rows per kv head (M = 4, GQA 8), the tcgen05 kernel
+    # r32: 32 query rows per kv head (M = 4, GQA 8) over 6 sequences: row groups
     c = upload(WORKLOADS[name] if name != "r32" else
                custom("noalloc_r32", 6, 4, 16, 2, ("uniform", 200, 3000), outliers=True))
     ref = run(c).cpu().numpy()                  # kattn_decode, caller-owned workspace
