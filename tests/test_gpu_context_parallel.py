@@ -11,7 +11,7 @@ another.
 import numpy as np
 import pytest
 
-from helpers import assert_f32_tolerance, custom, oracle_decode, run, upload
+from helpers import assert_f32_tolerance, custom, device_upload, oracle_decode, run, upload
 from int8_kv_decode_gb300 import context_parallel as cp
 from synth import WORKLOADS
 
@@ -91,14 +91,18 @@ def test_spec_verify_shards_equal_single_gpu_bytes(n_shards, p_mode):
     assert K.get_device_status(mws) == 0
 
 
-@pytest.mark.parametrize("n_shards", [2, 3])
-def test_r32_shards_equal_single_gpu_bytes(n_shards):
-    # 32 query rows per kv head (M = 4, GQA 8; 8 sequences: row groups): the
-    # window partials in shard mode, gathered and merged, give the single-GPU
-    # bytes.
+@pytest.mark.parametrize("n_shards,B", [(2, 8), (3, 8), (2, 48)])
+def test_r32_shards_equal_single_gpu_bytes(n_shards, B):
+    # 32 query rows per kv head (M = 4, GQA 8): the window partials in shard
+    # mode, gathered and merged, give the single-GPU bytes.  8 sequences take
+    # row groups; 48 long ones (more work items than the row-group bound) the
+    # tcgen05 kernel.
     import int8_kv_decode_gb300 as K
-    wl = custom("cp_r32", 8, 4, 16, 2, ("uniform", 300, 5000), outliers=True)
-    c = upload(wl)
+    if B <= 8:
+        c = upload(custom("cp_r32", B, 4, 16, 2, ("uniform", 300, 5000), outliers=True))
+    else:
+        c = device_upload(custom("cp_r32_big", B, 4, 16, 2, ("uniform", 20000, 30000),
+                                 outliers=True))
     ref = run(c).cpu().numpy()
     out, mws = cp_decode(c, n_shards, seed=70 + n_shards)
     assert np.array_equal(bits(out.cpu().numpy()), bits(ref))
