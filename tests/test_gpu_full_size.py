@@ -17,14 +17,17 @@ must hold the same bytes.
   size give the same bytes ("Kestrel_VLLM - 18", §二).
 * The fused KV append (the benchmark's step): the appended rows quantized by
   the oracle, the cache bytes and the decode against the oracle.
+* The tcgen05 kernel at 20 and 24 rows (many work items), and every rounded-P
+  mode on diffuse attention at 8k, where the rounding moves the output
+  measurably and the kernel must follow the same-rounding oracle.
 """
 
 import numpy as np
 import pytest
 
 import oracle
-from helpers import (ROUNDED_REL_L2, assert_f32_tolerance, bits, custom, device_case,
-                     oracle_sequence_cache, oracle_sequence_rows, pinned_tiling, rel_l2)
+from helpers import (ROUNDED_REL_L2, assert_f32_tolerance, bits, custom, device_case, oracle_decode,
+                     oracle_sequence_cache, oracle_sequence_rows, pinned_tiling, rel_l2, upload)
 from synth import WORKLOADS, make_workload
 
 pytestmark = pytest.mark.gpu
@@ -264,3 +267,28 @@ def test_tcgen05_kernel_at_24_and_20_rows(g, M):
             got.append(out[b, j, h])
             ref.append(o[j, h])
     _compare(np.array(got), np.array(ref), 0)
+
+
+@pytest.mark.parametrize("p_mode", [1, 2, 3, 4, 5])
+def test_rounded_p_acts_on_diffuse_attention_at_8k(p_mode):
+    # No outlier channels: attention spreads over thousands of keys, so every
+    # rounded-P mode moves the output measurably.  The kernel must sit within
+    # the rounded-mode bound of the oracle with the same rounding, and far
+    # closer to it than to the unrounded (f32 P) oracle.
+    import int8_kv_decode_gb300 as K
+    C, Bk = pinned_tiling()
+    wl = custom("diffuse_8k", 2, 1, 32, 4, 8192, outliers=False, index=41)
+    c = upload(wl)
+    got = K.decode(c.q, c.k8, c.ks, c.v8, c.vs, c.rs, c.ctx, c.x.max_ctx,
+                   p_mode=p_mode).cpu().numpy()
+    rows = [(b, 0, h) for b in range(wl.B) for h in (0, 7, 13, 20, 31)]
+    same = oracle_decode(c, rows=rows, p_mode=p_mode, C=C, Bk=Bk)
+    plain = oracle_decode(c, rows=rows)
+    m = np.zeros(got.shape[:3], bool)
+    for (b, j, h) in rows:
+        m[b, j, h] = True
+    effect = rel_l2(same[m], plain[m])
+    dist = rel_l2(got[m], same[m])
+    assert dist <= ROUNDED_REL_L2, dist
+    assert effect > 1e-5, effect
+    assert dist < 0.25 * effect, (dist, effect)
