@@ -100,11 +100,21 @@ def roofline_kernel(g: int, M: int, exact: bool, B: int = 1 << 20, max_ctx: int 
     return "decode_tc_kernel" if 16 < R <= 32 else "decode_fast_kernel"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and with whitespace collapsed, so that
+    an edit of a comment does not change a kernel's hash."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha(kernel: str = "decode_fast_kernel", paged: bool = False) -> str:
+    """Hash of the code (comments dropped) of the files a decode kernel is built from."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel] + (["decode_fast_paged.cu"] if paged else []):
-        with open(os.path.join(ROOT, "int8_kv_decode_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "int8_kv_decode_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,7 +14,11 @@
 //      the kv head -- the GQA group times the M draft columns -- so every K/V
 //      byte is read from HBM once.  The four spans are merged in a fixed
 //      pairwise order; a sequence of one window is finished here, otherwise
-//      the window's (m, l, o) goes to the workspace;
+//      the window's (m, l, o) goes to the workspace.  With more than 8 rows
+//      and few items (a small batch), each item is instead split into row
+//      groups of 8 rows, one CTA each of the one-tile variant, which read the
+//      same K/V blocks (all but the first from L2) and write their rows of
+//      the same window partial;
 //   3. merge_windows_kernel combines the windows of each row in order.
 //
 // Per warp and block of kBlockBk = 32 keys ("在 agent 时代如何快速验证 kernel
