@@ -117,3 +117,13 @@ def test_paged_rows_and_traffic_key():
     assert got.tolist() == [96, 33, 128, 5]
     assert bench.traffic_key("serving_b256_m4", 64) == "serving_b256_m4_paged64"
     assert bench.traffic_key("serving_b256_m4") == "serving_b256_m4"
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    import bench
+    src = "int f(int x) {  // the answer\n  return x + 1; /* one */\n}\n"
+    same = "int f(int x) {\n  // changed words\n  return x + 1;\n}\n"
+    other = "int f(int x) { return x + 2; }"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(other)
+    assert len(bench.kernel_source_sha("decode_fast_kernel")) == 16
