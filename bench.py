@@ -442,30 +442,34 @@ def run_ours(args):
     pm = K.P_MODES[args.p_mode]
     exact = bool(args.exact)
 
-    def decode(i):
+    # The step's inputs (the queries, the new K/V rows, their cache rows and
+    # the context lengths) and its output; the caches stay resident.
+    io0 = dict(q=q, knew=knew, vnew=vnew, ctx=ctx, dst=dst, out=out)
+
+    def decode(i, io=io0):
         k8, ks, v8, vs = caches[i % n_copies]
         if P:
-            K.decode_paged(q, k8, ks, v8, vs, bt, P, ctx, max_ctx, out=out,
+            K.decode_paged(io["q"], k8, ks, v8, vs, bt, P, io["ctx"], max_ctx, out=io["out"],
                            workspace=None if exact else ws, p_mode=pm, exact_mode=exact)
             return
-        K.decode(q, k8, ks, v8, vs, rs, ctx, max_ctx, out=out, workspace=None if exact else ws,
-                 p_mode=pm, exact_mode=exact)
+        K.decode(io["q"], k8, ks, v8, vs, rs, io["ctx"], max_ctx, out=io["out"],
+                 workspace=None if exact else ws, p_mode=pm, exact_mode=exact)
 
-    def step(i):
+    def step(i, io=io0):
         k8, ks, v8, vs = caches[i % n_copies]
         if exact:
             # exact mode has no fused append: the two appends, then the decode
-            K.quantize_kv_rows(knew, dst, k8, ks)
-            K.quantize_kv_rows(vnew, dst, v8, vs)
-            decode(i)
+            K.quantize_kv_rows(io["knew"], io["dst"], k8, ks)
+            K.quantize_kv_rows(io["vnew"], io["dst"], v8, vs)
+            decode(i, io)
             return
         # this step's K/V rows appended inside the decode call
         if P:
-            K.decode_paged_append(q, knew, vnew, dst, k8, ks, v8, vs, bt, P, ctx, max_ctx,
-                                  out=out, workspace=ws, p_mode=pm)
+            K.decode_paged_append(io["q"], io["knew"], io["vnew"], io["dst"], k8, ks, v8, vs, bt,
+                                  P, io["ctx"], max_ctx, out=io["out"], workspace=ws, p_mode=pm)
             return
-        K.decode_append(q, knew, vnew, dst, k8, ks, v8, vs, rs, ctx, max_ctx, out=out,
-                        workspace=ws, p_mode=pm)
+        K.decode_append(io["q"], io["knew"], io["vnew"], io["dst"], k8, ks, v8, vs, rs,
+                        io["ctx"], max_ctx, out=io["out"], workspace=ws, p_mode=pm)
 
     for i in range(args.warmup):
         step(i)
@@ -547,29 +551,47 @@ def run_ours(args):
 
     total_bytes, total_q, tmax = aggregate(kvb * args.steps, B * M * args.steps, elapsed, pg)
 
-    # End to end through the public API: inputs from pinned host memory each
-    # step, the result read back to the host each step.
-    h_q = q.cpu().pin_memory()
-    h_knew, h_vnew = knew.cpu().pin_memory(), vnew.cpu().pin_memory()
-    h_ctx = ctx.cpu().pin_memory()
-    h_dst = dst.cpu().pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = (h_q.numel() * 4 + h_knew.numel() * 4 + h_vnew.numel() * 4 + h_ctx.numel() * 4
-           + h_dst.numel() * 8)
-    d2h = h_out.numel() * 4
+    # End to end through the public API: every step's inputs copied from
+    # pinned host memory, every step's output read back to pinned host
+    # memory.  As a serving loop does, the copies run on their own streams
+    # against two sets of device buffers, so that step i + 1's inputs arrive
+    # and step i - 1's output leaves while step i computes; a buffer is
+    # refilled only after the step that used it is done and its output is out.
+    host = {k: io0[k].cpu().pin_memory() for k in ("q", "knew", "vnew", "ctx", "dst")}
+    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_outs[0].numel() * 4
+    bufs = [io0] + [{k: torch.empty_like(v) for k, v in io0.items()}]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # buffer b's inputs landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # the step on buffer b is done
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # buffer b's output is on the host
     torch.cuda.synchronize(dev)
     if pg is not None:
         dist.barrier()
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
+    s_in.wait_event(e_start)
+    s_out.wait_event(e_start)
     for i in range(args.steps):
-        q.copy_(h_q, non_blocking=True)
-        knew.copy_(h_knew, non_blocking=True)
-        vnew.copy_(h_vnew, non_blocking=True)
-        ctx.copy_(h_ctx, non_blocking=True)
-        dst.copy_(h_dst, non_blocking=True)
-        step(i)
-        h_out.copy_(out, non_blocking=True)
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_done[b])            # step i - 2 has read buffer b
+            for k, t in host.items():
+                bufs[b][k].copy_(t, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])               # step i - 2's output has left
+        step(i, bufs[b])
+        ev_done[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[b])
+            h_outs[b].copy_(bufs[b]["out"], non_blocking=True)
+            ev_out[b].record(s_out)
+    for b in range(min(2, args.steps)):
+        stream.wait_event(ev_out[b])
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     e_elapsed = e_start.elapsed_time(e_end) / 1e3
