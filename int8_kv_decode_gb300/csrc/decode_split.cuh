@@ -227,10 +227,13 @@ __device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, ui
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// 2^x by the SFU (ex2.approx; subnormal results kept, 2^-inf = +0).
+// 2^x by the SFU in one instruction (ex2.approx.ftz: a result below 2^-126 is
+// flushed to +0, 2^-inf = +0).  Every fast-mode kernel takes its weights from
+// here, so the flush is the same for a row whatever kernel reduces it; a
+// weight that small is below 1e-38 of the row's largest and moves no output.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
 
