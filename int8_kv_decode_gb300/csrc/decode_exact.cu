@@ -20,15 +20,8 @@ namespace {
 
 constexpr int kChunk = 128;
 constexpr int kSub = 32;                          // keys per step of the serial scan
-
-// f32 of a signed byte, exactly: the offset-binary byte u = v + 128 placed in
-// the low mantissa bits of 1.5 * 2^23 gives 12582912 + u; subtracting
-// 12582912 + 128 leaves v (both operands and the difference are integers
-// below 2^24, so nothing rounds).
-__device__ __forceinline__ float i8_to_f32(uint8_t byte) {
-  const uint32_t u = (uint32_t)(byte ^ 0x80u);
-  return __fsub_rn(__uint_as_float(0x4B400000u | u), 12583040.0f);
-}
+constexpr int kProducersBar = 128;                // threads of the producer group
+constexpr int kConsumersBar = 160;                // chains (128) and the row-sum warp
 
 // Table-driven float32 exp (P. T. P. Tang, ACM TOMS 1989; the variant the
 // page describes in §3.3): x = (64m + j + r/C2)/K, exp(x) = 2^m 2^(j/64) e^r,
@@ -88,47 +81,65 @@ __device__ __forceinline__ bool ex_mbar_wait(uint64_t* bar, uint32_t parity) {
   }
   return false;
 }
-// Barrier among the 128 threads of one group (ids 1 and 2; 0 is __syncthreads).
+// Barrier among the threads of one group: the producers (id 1) or the
+// consumers (id 2); 0 is __syncthreads.
 __device__ __forceinline__ void group_sync(int id) {
-  asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory");
+  if (id == 1) asm volatile("bar.sync 1, %0;\n" ::"n"(kProducersBar) : "memory");
+  else asm volatile("bar.sync 2, %0;\n" ::"n"(kConsumersBar) : "memory");
 }
 
 // Shared memory of one row's CTA.  A chunk's K and V rows are staged by
-// cp.async one chunk ahead (three stages); the 16-byte pieces of a K row sit at
+// cp.async one chunk ahead (two stages); the 16-byte pieces of a K row sit at
 // piece c ^ (key & 7) so that the per-key dot products read without bank
-// conflicts.  tok holds, per key of a stage: round_p(p), v_scale, alpha, p.
-constexpr int kStages = 3;                        // K/V stages: the chains may be a chunk behind
+// conflicts.  The producers then lay the chunk's V out by channel (vt: the
+// offset-binary bytes v + 128 of one channel for the chunk's 128 keys, 16-key
+// piece j at piece j ^ ((channel / 4) mod 8), so that both the transposing
+// stores and the chain threads' 16-byte loads spread over all bank groups).
+constexpr int kChainThreads = kD;                 // one per channel
+constexpr int kSumThreads = 32;                   // the warp that walks the row sum
+constexpr int kConsumers = kChainThreads + kSumThreads;
+constexpr int kProducers = kChunk;                // one per key of a chunk
+constexpr int kExactThreads = kConsumers + kProducers;
+constexpr int kSubs = kChunk / kSub;
 
 struct ExactSmem {
-  int8_t k[kStages][kChunk][kD];
-  int8_t v[kStages][kChunk][kD];
-  float4 tok[2][kChunk];
+  int8_t k[2][kChunk][kD];
+  uint8_t v[2][kChunk][kD];                       // as the cache holds them
+  uint8_t vt[2][kD][kChunk];                      // by channel, offset binary
+  float2 pv[2][kChunk];                           // per key: round_p(p), v_scale
+  float2 ap[2][kChunk];                           // per key: alpha, p
+  int same[2][kSubs];                             // every alpha of the 32 keys is exactly 1
   ExpfConsts c;
-  uint64_t full[2];                               // chunk c's tok (and V) are ready: full[c & 1]
+  uint64_t full[2];                               // chunk c's pv, ap, same, vt are ready: full[c & 1]
   uint64_t empty[2];                              // the chains are done with chunk c: empty[c & 1]
-  int row[kStages][kChunk];                       // plane rows of the stage's keys
+  int row[2][kChunk];                             // plane rows of the stage's keys
   uint32_t q8[kD / 4];
   float red[kChunk / 32];
   float carry;
+  float lsum;                                     // the row sum, for the final division
   int ok_p, ok_c;                                 // group-wide outcome of a bounded wait
 };
 
-// One CTA of 256 threads per query row, in two groups that overlap chunks:
-//   producers (threads 128..255, one per key of a chunk): stage chunk c + 1,
-//     then chunk c's scores, prefix max and exps -> tok[c & 1];
-//   chains (threads 0..127, one per channel): walk chunk c's o and l chains
-//     while the producers work on chunk c + 1.
+// One CTA of 288 threads per query row, in two groups that overlap chunks:
+//   producers (128 threads, one per key of a chunk): stage chunk c + 1, then
+//     chunk c's scores, prefix max and exps -> pv, ap [c & 1], and chunk c's
+//     V by channel -> vt[c & 1];
+//   consumers: the chains (128 threads, one per channel) walk chunk c's o
+//     chain and one warp its l chain, while the producers work on chunk c + 1.
 // A stage is handed over through full / empty mbarriers; one thread of each
 // group waits (bounded) and the group learns the outcome at a group barrier.
-__global__ void __launch_bounds__(2 * kChunk)
+//
+// Where every alpha of a run of 32 keys is exactly 1 (the running max did not
+// move), the chain steps o = o * alpha + term and l = l * alpha + p are taken
+// as o = o + term and l = l + p: multiplying by 1 is exact, so the bits are
+// the same and each step is one rounding shorter.
+__global__ void __launch_bounds__(kExactThreads)
 decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   extern __shared__ __align__(16) unsigned char exact_smem[];
   ExactSmem& sm = *reinterpret_cast<ExactSmem*>(exact_smem);
 
   const int tid = threadIdx.x;
-  const bool producer = tid >= kChunk;
-  const int gt = producer ? tid - kChunk : tid;   // key (producers) or channel (chains)
-  const int lane = gt & 31, gwarp = gt >> 5;
+  const bool producer = tid >= kConsumers;
   const int h = blockIdx.x % p.Hq;
   const int j = (blockIdx.x / p.Hq) % p.M;
   const int b = blockIdx.x / (p.Hq * p.M);
@@ -137,7 +148,7 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   float* orow = p.out + qrow * kD;
 
   if (!sequence_valid(p, b)) {
-    if (!producer) orow[gt] = __int_as_float(0x7fc00000);
+    if (tid < kChainThreads) orow[tid] = __int_as_float(0x7fc00000);
     if (tid == 0 && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_BAD_SEQUENCE);
     return;
   }
@@ -145,7 +156,7 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   const int rs = sequence_row0(p, b);
   const int nchunks = (L + kChunk - 1) / kChunk;
 
-  for (int i = tid; i < (int)(sizeof(ExpfConsts) / sizeof(double)); i += 2 * kChunk)
+  for (int i = tid; i < (int)(sizeof(ExpfConsts) / sizeof(double)); i += kExactThreads)
     reinterpret_cast<double*>(&sm.c)[i] = reinterpret_cast<const double*>(&consts)[i];
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -166,6 +177,8 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
 
   if (producer) {
     // ---------------------------------------------------------- producers
+    const int gt = tid - kConsumers;              // key of the chunk
+    const int lane = gt & 31, gwarp = gt >> 5;
     float ks_next = 0.0f, vs_next = 0.0f;
     auto stage_rows = [&](int t0, int st) {
       const int t = t0 + gt;
@@ -195,7 +208,8 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
     group_sync(1);
     issue(0, 0);
 
-    // int8 query: absmax over the 128 channels, then one IEEE division each.
+    // int8 query: absmax over the 128 channels, then one IEEE division each;
+    // every producer then keeps the whole quantized row in registers.
     const float x = p.q[qrow * kD + gt];
     float amax = warp_max(fabsf(x));
     if (lane == 0) sm.red[gwarp] = amax;
@@ -204,14 +218,17 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
     const float qs = quant_scale(amax);
     reinterpret_cast<int8_t*>(sm.q8)[gt] = (int8_t)quant_one(x, qs);
     group_sync(1);                                // q8 complete; red free again
+    uint32_t q8[kD / 4];
+#pragma unroll
+    for (int w = 0; w < kD / 4; ++w) q8[w] = sm.q8[w];
 
     for (int c = 0; c < nchunks; ++c) {
-      const int st = c % kStages, tb = c & 1, t0 = c * kChunk, t = t0 + gt;
+      const int st = c & 1, tb = st, t0 = c * kChunk, t = t0 + gt;   // K/V stage, buffers
       const bool live = t < L;
       const int n = min(kChunk, L - t0);
       const float ks_cur = ks_next, vs_cur = vs_next;
-      // The chains must be done with chunk c - 2: its K/V stage takes chunk
-      // c + 1 now, and its tok buffer takes chunk c.
+      // The consumers must be done with chunk c - 2: its pv, ap and vt
+      // buffers take chunk c.
       if (c >= 2) {
         if (gt == 0) {
           sm.ok_p = ex_mbar_wait(&sm.empty[tb], ((c - 2) >> 1) & 1);
@@ -220,10 +237,12 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
         group_sync(1);
         if (!sm.ok_p) break;                      // the copies in flight drain below
       }
+      // Stage chunk c + 1 into the K/V stage chunk c - 1 left (read only by
+      // this group, before the barrier that ended the previous chunk).
       if (c + 1 < nchunks) {
-        stage_rows(t0 + kChunk, (c + 1) % kStages);
+        stage_rows(t0 + kChunk, st ^ 1);
         group_sync(1);
-        issue(t0 + kChunk, (c + 1) % kStages);
+        issue(t0 + kChunk, st ^ 1);
       } else {
         cp_async_commit();                        // an empty group keeps the count
       }
@@ -232,16 +251,18 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
 
       float s = -INFINITY;
       if (live) {
+        // four partial sums (integers: any order gives the same total)
         const int4* krow = reinterpret_cast<const int4*>(sm.k[st][gt]);
-        int acc = 0;
+        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
 #pragma unroll
         for (int cc = 0; cc < kD / 16; ++cc) {
           const int4 kv = krow[cc ^ (gt & 7)];
-          acc = __dp4a((int)kv.x, (int)sm.q8[4 * cc + 0], acc);
-          acc = __dp4a((int)kv.y, (int)sm.q8[4 * cc + 1], acc);
-          acc = __dp4a((int)kv.z, (int)sm.q8[4 * cc + 2], acc);
-          acc = __dp4a((int)kv.w, (int)sm.q8[4 * cc + 3], acc);
+          a0 = __dp4a((int)kv.x, (int)q8[4 * cc + 0], a0);
+          a1 = __dp4a((int)kv.y, (int)q8[4 * cc + 1], a1);
+          a2 = __dp4a((int)kv.z, (int)q8[4 * cc + 2], a2);
+          a3 = __dp4a((int)kv.w, (int)q8[4 * cc + 3], a3);
         }
+        const int acc = (a0 + a1) + (a2 + a3);
         s = __fmul_rn(__fmul_rn((float)acc, __fmul_rn(qs, ks_cur)), p.sm_scale);
       }
       // Inclusive prefix max over the chunk, seeded with the running max.
@@ -264,14 +285,48 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
         for (int w = 0; w < gwarp; ++w) pw = fmaxf(pw, sm.red[w]);
         prev = pw;
       }
+      float a = 1.0f;
       if (live) {
         // expf_tang(0) is exactly 1: skip the double-precision steps when the
         // running max did not move.
-        const float a = prev == pm ? 1.0f : expf_tang(__fsub_rn(prev, pm), sm.c);
+        a = prev == pm ? 1.0f : expf_tang(__fsub_rn(prev, pm), sm.c);
         const float pp = s == pm ? 1.0f : expf_tang(__fsub_rn(s, pm), sm.c);
-        sm.tok[tb][gt] = make_float4(round_p_exact(pp, p.p_mode), vs_cur, a, pp);
+        sm.pv[tb][gt] = make_float2(round_p_exact(pp, p.p_mode), vs_cur);
+        sm.ap[tb][gt] = make_float2(a, pp);
       }
-      group_sync(1);                              // tok complete; red and carry reads done
+      // warp gwarp holds keys 32 gwarp .. + 31: its run of alphas
+      const bool same = __all_sync(0xffffffffu, a == 1.0f);
+      if (lane == 0) sm.same[tb][gwarp] = same ? 1 : 0;
+      // Chunk c's V by channel: thread (kb = gwarp, g4 = lane) transposes keys
+      // 32 kb .. + 31 of channels 4 g4 .. + 3, in 4 x 4 byte blocks.
+      {
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          w[k] = *reinterpret_cast<const uint32_t*>(&sm.v[st][32 * gwarp + k][4 * lane]);
+        uint32_t ot[4][8];                        // [channel i][keys 4q .. 4q + 3]
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t t01 = __byte_perm(w[4 * q], w[4 * q + 1], 0x5140);
+          const uint32_t t23 = __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x5140);
+          const uint32_t u01 = __byte_perm(w[4 * q], w[4 * q + 1], 0x7362);
+          const uint32_t u23 = __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x7362);
+          ot[0][q] = __byte_perm(t01, t23, 0x5410) ^ 0x80808080u;
+          ot[1][q] = __byte_perm(t01, t23, 0x7632) ^ 0x80808080u;
+          ot[2][q] = __byte_perm(u01, u23, 0x5410) ^ 0x80808080u;
+          ot[3][q] = __byte_perm(u01, u23, 0x7632) ^ 0x80808080u;
+        }
+        const int sw = lane & 7;                  // (channel / 4) mod 8
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int piece = (2 * gwarp + hh) ^ sw;
+            *reinterpret_cast<uint4*>(&sm.vt[tb][4 * lane + i][16 * piece]) =
+                make_uint4(ot[i][4 * hh], ot[i][4 * hh + 1], ot[i][4 * hh + 2], ot[i][4 * hh + 3]);
+          }
+      }
+      group_sync(1);                              // chunk c published; red and carry reads done
       if (gt == n - 1) sm.carry = pm;
       if (gt == 0) ex_mbar_arrive(&sm.full[tb]);
     }
@@ -279,12 +334,15 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
     return;
   }
 
-  // ---------------------------------------------------------------- chains
-  float o = 0.0f, l = 0.0f;
+  // -------------------------------------------------------------- consumers
+  const bool chain = tid < kChainThreads;         // else the row-sum warp
+  const int ch = tid;                             // chains: the channel
+  const int sw = (ch >> 2) & 7;
+  float acc = 0.0f;                               // o (chains) or l (row-sum warp)
   bool ok = true;
   for (int c = 0; c < nchunks; ++c) {
-    const int st = c % kStages, tb = c & 1, n = min(kChunk, L - c * kChunk);
-    if (gt == 0) {
+    const int tb = c & 1, n = min(kChunk, L - c * kChunk);
+    if (tid == 0) {
       sm.ok_c = ex_mbar_wait(&sm.full[tb], (c >> 1) & 1);
       if (!sm.ok_c && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
     }
@@ -293,39 +351,65 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
       ok = false;
       break;
     }
-    // 32 keys at a time: first every key's term round_p(p) * (f32(v8) * vs)
-    // (independent of one another), then the two chains, key by key.
-    const uint8_t* vcol = reinterpret_cast<const uint8_t*>(&sm.v[st][0][gt]);
-    const float2* tk2 = reinterpret_cast<const float2*>(sm.tok[tb]);
-    for (int u0 = 0; u0 < n; u0 += kSub) {
-      float term[kSub];
-#pragma unroll
-      for (int i = 0; i < kSub; ++i) {
-        const float2 pv = tk2[2 * (u0 + i)];      // round_p(p), v_scale
-        term[i] = __fmul_rn(pv.x, __fmul_rn(i8_to_f32(vcol[(u0 + i) * kD]), pv.y));
-      }
-      if (u0 + kSub <= n) {
+    const float2* pvb = sm.pv[tb];
+    const float2* apb = sm.ap[tb];
+    for (int sb = 0; sb * kSub < n; ++sb) {
+      const int u0 = sb * kSub;
+      const bool full_run = u0 + kSub <= n;
+      const bool same = sm.same[tb][sb] != 0;
+      if (chain) {
+        // this channel's 32 bytes: keys u0 .. u0 + 31, byte i of word i / 4
+        const uint4 va = *reinterpret_cast<const uint4*>(&sm.vt[tb][ch][16 * ((2 * sb) ^ sw)]);
+        const uint4 vb = *reinterpret_cast<const uint4*>(&sm.vt[tb][ch][16 * ((2 * sb + 1) ^ sw)]);
+        const uint32_t vw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+        // every key's term round_p(p) * (f32(v8) * vs) first (independent of
+        // one another): the offset-binary byte u in the low mantissa bits of
+        // 1.5 * 2^23 gives 12582912 + u, minus 12582912 + 128 leaves v exactly
+        float term[kSub];
 #pragma unroll
         for (int i = 0; i < kSub; ++i) {
-          const float2 ap = tk2[2 * (u0 + i) + 1];   // alpha, p
-          o = __fadd_rn(__fmul_rn(o, ap.x), term[i]);
-          l = __fadd_rn(__fmul_rn(l, ap.x), ap.y);
+          const float2 pvv = pvb[u0 + i];
+          const float vf = __fsub_rn(__uint_as_float(__byte_perm(vw[i >> 2], 0x4B400000u, 0x7640u | (i & 3))),
+                                     12583040.0f);
+          term[i] = __fmul_rn(pvv.x, __fmul_rn(vf, pvv.y));
+        }
+        if (full_run && same) {
+#pragma unroll
+          for (int i = 0; i < kSub; ++i) acc = __fadd_rn(acc, term[i]);
+        } else if (full_run) {
+#pragma unroll
+          for (int i = 0; i < kSub; ++i) acc = __fadd_rn(__fmul_rn(acc, apb[u0 + i].x), term[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kSub; ++i)
+            if (u0 + i < n) acc = __fadd_rn(__fmul_rn(acc, apb[u0 + i].x), term[i]);
         }
       } else {
+        if (full_run && same) {
 #pragma unroll
-        for (int i = 0; i < kSub; ++i) {
-          if (u0 + i < n) {
-            const float2 ap = tk2[2 * (u0 + i) + 1];
-            o = __fadd_rn(__fmul_rn(o, ap.x), term[i]);
-            l = __fadd_rn(__fmul_rn(l, ap.x), ap.y);
+          for (int i = 0; i < kSub; ++i) acc = __fadd_rn(acc, apb[u0 + i].y);
+        } else if (full_run) {
+#pragma unroll
+          for (int i = 0; i < kSub; ++i) {
+            const float2 x2 = apb[u0 + i];
+            acc = __fadd_rn(__fmul_rn(acc, x2.x), x2.y);
           }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kSub; ++i)
+            if (u0 + i < n) {
+              const float2 x2 = apb[u0 + i];
+              acc = __fadd_rn(__fmul_rn(acc, x2.x), x2.y);
+            }
         }
       }
     }
     group_sync(2);                                // every chain is done with chunk c
-    if (gt == 0) ex_mbar_arrive(&sm.empty[tb]);
+    if (tid == 0) ex_mbar_arrive(&sm.empty[tb]);
   }
-  orow[gt] = ok ? __fdiv_rn(o, l) : __int_as_float(0x7fc00000);
+  if (tid == kChainThreads) sm.lsum = acc;
+  group_sync(2);
+  if (chain) orow[ch] = ok ? __fdiv_rn(acc, sm.lsum) : __int_as_float(0x7fc00000);
 }
 
 }  // namespace
@@ -337,7 +421,7 @@ cudaError_t launch_decode_exact(const DecodeParams& p, const ExpfConsts& c,
   cudaError_t e = cudaFuncSetAttribute(decode_exact_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_exact_kernel<<<(unsigned)rows, 2 * kChunk, smem, stream>>>(p, c);
+  decode_exact_kernel<<<(unsigned)rows, kExactThreads, smem, stream>>>(p, c);
   return cudaGetLastError();
 }
 
