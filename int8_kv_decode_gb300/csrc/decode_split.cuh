@@ -389,6 +389,32 @@ __device__ __forceinline__ Item load_unit(const DecodeParams& p, int t, int tota
   return it;
 }
 
+// A unit's work item as loaded, not yet taken apart: a kernel fetches the
+// unit two items ahead and decodes it one item later, so that no warp waits
+// on the load at an item boundary.
+struct RawUnit {
+  int4 v;
+  int rg;
+  bool valid;
+};
+
+__device__ __forceinline__ RawUnit fetch_unit(const DecodeParams& p, int t, int total, int nrg) {
+  RawUnit r{make_int4(0, 0, 0, 0), 0, false};
+  const int i = nrg == 1 ? t : t / nrg;
+  if (i < total) {
+    r.v = __ldcg(p.items + i);
+    r.rg = t - i * nrg;
+    r.valid = true;
+  }
+  return r;
+}
+
+__device__ __forceinline__ Item decode_unit(const RawUnit& r) {
+  Item it{-1, 0, 0, 0, 0, 0};
+  if (r.valid) it = Item{r.v.x & 0xffff, (int)((unsigned)r.v.x >> 16), r.v.y, r.v.z, r.v.w, r.rg};
+  return it;
+}
+
 // Keys [s0, s1) of span kw of the item's window, its nb blocks, and the cache
 // row of key s0 in the 2-D view [Hkv * cap_rows][128] (contiguous layout).
 struct Span {
@@ -503,8 +529,8 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   const int G = gridDim.x;
   int t = blockIdx.x;
   if (t >= units) return;
-  Item it0 = load_unit(p, t, total, nrg), it1 = load_unit(p, t + G, total, nrg),
-       it2 = load_unit(p, t + 2 * G, total, nrg);
+  Item it0 = load_unit(p, t, total, nrg), it1 = load_unit(p, t + G, total, nrg);
+  RawUnit raw2 = fetch_unit(p, t + 2 * G, total, nrg);   // decoded one item later
   if (nrg > 1) place_rows(it0.rg);
 
   bool q_pending = false;                         // thread 0: a query copy in flight
@@ -530,18 +556,37 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   int par = 0;                                    // item parity: (m, l) and block-row buffers
   // Paged layout: the producer warp looks up the cache rows (2-D view) of its
   // span's blocks one item ahead, into the slot of the item's parity (lane e:
-  // block e; a block never crosses a page).
-  auto block_rows = [&](const Item& it, int slot) {
+  // block e; a block never crosses a page).  At an item boundary it only
+  // loads the next item's table entries (rows_ahead); they become rows when
+  // the producer reaches that item (rows_finish), so no warp waits there.
+  int pg_entry = 0, pg_key = 0, pg_n = 0, pg_slot = 0, pg_row = 0;
+  bool pg_pending = false;
+  auto rows_ahead = [&](const Item& it, int slot) {
     if constexpr (PG) {
       if (producer && it.b >= 0) {
         const Span s = span_of(it, kw, M);
-        if (lane < s.nb) sm.brow[kw][slot][lane] = it.row + paged_row(p, it.b, s.s0 + lane * kBlockBk);
-        __syncwarp();
+        pg_key = s.s0 + lane * kBlockBk;
+        if (lane < s.nb) pg_entry = page_entry(p, it.b, pg_key);
+        pg_n = s.nb;
+        pg_slot = slot;
+        pg_row = it.row;
+        pg_pending = true;
       }
     }
   };
-  block_rows(it0, 0);
-  block_rows(it1, 1);
+  auto rows_finish = [&]() {
+    if constexpr (PG) {
+      if (pg_pending) {
+        if (lane < pg_n) sm.brow[kw][pg_slot][lane] = pg_row + page_row_of(p, pg_entry, pg_key);
+        __syncwarp();
+        pg_pending = false;
+      }
+    }
+  };
+  rows_ahead(it0, 0);
+  rows_finish();
+  rows_ahead(it1, 1);
+  rows_finish();
   uint32_t used = 0, eph = 0;                     // NG > 1: stages filled before; empty parities
   const uint64_t kv_policy = nrg > 1 ? l2_evict_normal() : l2_evict_first();
   // Returns false if a stage was never released (a bounded wait ran out).
@@ -568,6 +613,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
         ++inflight;
         ist = ist + 1 == kRing ? 0 : ist + 1;
       } else if (pitem == 0 && it1.b >= 0) {
+        rows_finish();                            // the next item's rows, loaded ahead
         pitem = 1;
         pblk = 0;
         psp = span_of(it1, kw, M);
@@ -993,8 +1039,8 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     t += G;
     if (t >= units) break;
     it0 = it1;
-    it1 = it2;
-    it2 = load_unit(p, t + 2 * G, total, nrg);
+    it1 = decode_unit(raw2);
+    raw2 = fetch_unit(p, t + 2 * G, total, nrg);
     if (nrg > 1) place_rows(it0.rg);
     sp = span_of(it0, kw, M);
 #pragma unroll
@@ -1005,7 +1051,7 @@ decode_fast_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     load_span_scales<PG>(p, it1, span_of(it1, kw, M), lane, ksn, vsn);
     qph ^= 1u;
     par ^= 1;
-    block_rows(it1, par ^ 1);                     // the slot the producer has left
+    rows_ahead(it1, par ^ 1);                     // the slot the producer has left
     if (pitem == 1) {
       pitem = 0;                                  // the producer is already on this item
     } else {

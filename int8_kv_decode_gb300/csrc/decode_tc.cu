@@ -101,6 +101,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
   uint32_t qph = 0;
   bool failed = false, q_pending = false;
   Item it = load_item(p, blockIdx.x, total), nxt = load_item(p, blockIdx.x + G, total);
+  RawUnit raw = fetch_unit(p, blockIdx.x + 2 * G, total, 1);   // decoded one item later
   int nbs[kSpansPerCta], nbs_n[kSpansPerCta], nbt = 0, nbt_n = 0;
   auto blocks_of = [&](const Item& x, int (&n)[kSpansPerCta]) {
     int tot = 0;
@@ -508,7 +509,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
     }
     gbase += nbt;
     it = nxt;
-    nxt = load_item(p, t + 2 * G, total);
+    nxt = decode_unit(raw);
+    raw = fetch_unit(p, t + 3 * G, total, 1);
     par ^= 1;
   }
 

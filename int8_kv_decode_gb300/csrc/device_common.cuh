@@ -115,13 +115,21 @@ __device__ __forceinline__ bool sequence_valid(const DecodeParams& p, int b) {
 // Row of key `key` of sequence b within its kv-head plane (paged layout).  An
 // entry outside the cache sets KATTN_DEVERR_BAD_PAGE and reads page 0, so no
 // access leaves the arrays.
-__device__ __forceinline__ int paged_row(const DecodeParams& p, int b, int key) {
-  int page = __ldg(p.block_table + (int64_t)b * p.max_pages + (key >> p.page_shift));
+// The block-table entry of a key, and the row that entry gives it (an entry
+// outside the plane flags KATTN_DEVERR_BAD_PAGE and reads page 0): apart, so
+// that a caller can load the entry well before it needs the row.
+__device__ __forceinline__ int page_entry(const DecodeParams& p, int b, int key) {
+  return __ldg(p.block_table + (int64_t)b * p.max_pages + (key >> p.page_shift));
+}
+__device__ __forceinline__ int page_row_of(const DecodeParams& p, int page, int key) {
   if ((unsigned)page >= (unsigned)p.n_pages) {
     if (p.err_word) atomicOr(p.err_word, KATTN_DEVERR_BAD_PAGE);
     page = 0;
   }
   return (page << p.page_shift) | (key & ((1 << p.page_shift) - 1));
+}
+__device__ __forceinline__ int paged_row(const DecodeParams& p, int b, int key) {
+  return page_row_of(p, page_entry(p, b, key), key);
 }
 
 // Row of key 0 of sequence b within its plane: the contiguous layout's
