@@ -270,26 +270,50 @@ merge_windows_kernel(const DecodeParams p) {
       }
     }
   } else {
-    // warp k = slot k: windows k, k + 32, ...
+    // warp k = slot k: windows k, k + 32, ...  The slot's first kPre windows
+    // (m, l and o) are loaded at once, before the maximum is known.
+    constexpr int kPre = 4;
+    float4 vp[kPre];
+    float mp[kPre], lp[kPre];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+      const int s = warp + kMergeSlots * i;
+      if (s < ns) {
+        mp[i] = __ldcg(mcol + woff(s));
+        lp[i] = __ldcg(lcol + woff(s));
+        vp[i] = ldo(s);
+      }
+    }
     float mloc = -INFINITY;
-    for (int s = warp; s < ns; s += kMergeSlots) mloc = fmaxf(mloc, __ldcg(mcol + woff(s)));
+#pragma unroll
+    for (int i = 0; i < kPre; ++i)
+      if (warp + kMergeSlots * i < ns) mloc = fmaxf(mloc, mp[i]);
+    for (int s = warp + kMergeSlots * kPre; s < ns; s += kMergeSlots) mloc = fmaxf(mloc, __ldcg(mcol + woff(s)));
     if (lane == 0) sm_red[warp] = mloc;
     __syncthreads();
     const float M = warp_max(sm_red[lane]);     // the 32 slot maxima (-inf for empty slots)
     float4 in = make_float4(0.f, 0.f, 0.f, 0.f);
     float il = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+      if (warp + kMergeSlots * i < ns) {
+        const float w = exp_diff(mp[i], M);
+        if (i == 0) {
+          in = mul4(w, vp[i]);
+          il = __fmul_rn(w, lp[i]);
+        } else {
+          in = fma4(w, vp[i], in);
+          il = __fmaf_rn(w, lp[i], il);
+        }
+      }
+    }
 #pragma unroll 4
-    for (int s = warp; s < ns; s += kMergeSlots) {
+    for (int s = warp + kMergeSlots * kPre; s < ns; s += kMergeSlots) {
       const float w = exp_diff(__ldcg(mcol + woff(s)), M);
       const float ls = __ldcg(lcol + woff(s));
       const float4 v = ldo(s);
-      if (s == warp) {
-        in = mul4(w, v);
-        il = __fmul_rn(w, ls);
-      } else {
-        in = fma4(w, v, in);
-        il = __fmaf_rn(w, ls, il);
-      }
+      in = fma4(w, v, in);
+      il = __fmaf_rn(w, ls, il);
     }
     sm_o[warp][lane] = in;
     if (lane == 0) sm_l[warp] = il;
