@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kListThreads) list_kernel(const DecodeParams p
 constexpr int kMergeSlots = 32;
 
 template <int WPR>
-__global__ void __launch_bounds__(WPR == 1 ? 256 : 32 * WPR, WPR == 1 ? 4 : 1)
+__global__ void __launch_bounds__(WPR == 1 ? 256 : 32 * WPR, WPR == 1 ? 3 : 1)
 merge_windows_kernel(const DecodeParams p) {
   constexpr int kRowsPerCta = WPR == 1 ? 8 : 1;
   __shared__ float sm_red[WPR == 1 ? 1 : kMergeSlots];
@@ -240,7 +240,19 @@ merge_windows_kernel(const DecodeParams p) {
   float4 O;
   float L;
   if constexpr (WPR == 1) {
-    // lane k: windows k and k + 32 (ns <= 64)
+    // lane k: windows k and k + 32 (ns <= 64).  The first batch of o loads
+    // goes out with the m and l loads, before the maximum is known.
+    const int nk = min(ns, kMergeSlots);
+    constexpr int kBatch = 4;                     // slots whose loads are in flight together
+    float4 a[kBatch], c[kBatch];
+    auto load_batch = [&](int k0) {
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (k0 + i < nk) a[i] = ldo(k0 + i);
+        if (k0 + i + kMergeSlots < ns) c[i] = ldo(k0 + i + kMergeSlots);
+      }
+    };
+    load_batch(0);
     const bool h0 = lane < ns, h1 = lane + kMergeSlots < ns;
     const float m0 = h0 ? __ldcg(mcol + woff(lane)) : -INFINITY;
     const float m1 = h1 ? __ldcg(mcol + woff(lane + kMergeSlots)) : -INFINITY;
@@ -249,16 +261,9 @@ merge_windows_kernel(const DecodeParams p) {
     const float M = warp_max(fmaxf(m0, m1));
     const float w0 = h0 ? exp_diff(m0, M) : 0.0f, w1 = h1 ? exp_diff(m1, M) : 0.0f;
     L = warp_sum(h1 ? __fmaf_rn(w1, l1, __fmul_rn(w0, l0)) : __fmul_rn(w0, l0));
-    const int nk = min(ns, kMergeSlots);
     O = make_float4(0.f, 0.f, 0.f, 0.f);
-    constexpr int kBatch = 4;                     // slots whose loads are in flight together
     for (int k0 = 0; k0 < nk; k0 += kBatch) {
-      float4 a[kBatch], c[kBatch];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        if (k0 + i < nk) a[i] = ldo(k0 + i);
-        if (k0 + i + kMergeSlots < ns) c[i] = ldo(k0 + i + kMergeSlots);
-      }
+      if (k0 > 0) load_batch(k0);
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
         const int k = k0 + i;
@@ -417,7 +422,7 @@ cudaError_t launch_decode_fast(const DecodeParams& p, cudaStream_t stream) {
 
 // The window merge (the same arithmetic in both shapes), over the windows of
 // at most n_shards * part_ws per row.  Estimated time = waves x dependent
-// loads per row: one warp per row (32 rows per SM at once; a load round per 4
+// loads per row: one warp per row (24 rows per SM at once; a load round per 4
 // windows) or 32 warps per row (one row per SM; a round per 128 windows), for
 // rows of up to 64 windows.
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
@@ -431,7 +436,7 @@ cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
       sms = 1;
   }
-  const int64_t est_warp = (all_rows + 32LL * sms - 1) / (32LL * sms) * ((nwin + 3) / 4 + 2);
+  const int64_t est_warp = (all_rows + 24LL * sms - 1) / (24LL * sms) * ((nwin + 3) / 4 + 2);
   const int64_t est_cta = (all_rows + sms - 1) / sms * ((nwin + 127) / 128 + 3);
   if (nwin <= 2 * kMergeSlots && est_warp <= est_cta)
     return launch_pdl(merge_windows_kernel<1>, dim3((unsigned)((rows_b + 7) / 8), (unsigned)p.B),
