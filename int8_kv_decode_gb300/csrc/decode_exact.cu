@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kChunk = 128;
 constexpr int kSub = 32;                          // keys per step of the serial scan
-constexpr int kProducersBar = 128;                // threads of the producer group
+constexpr int kProducersBar = 128;                // threads of one producer group
 constexpr int kConsumersBar = 160;                // chains (128) and the row-sum warp
 
 // Table-driven float32 exp (P. T. P. Tang, ACM TOMS 1989; the variant the
@@ -81,59 +81,66 @@ __device__ __forceinline__ bool ex_mbar_wait(uint64_t* bar, uint32_t parity) {
   }
   return false;
 }
-// Barrier among the threads of one group: the producers (id 1) or the
-// consumers (id 2); 0 is __syncthreads.
+// Barrier among the threads of one group: producer group 0 (id 1), the
+// consumers (id 2) or producer group 1 (id 3); 0 is __syncthreads.
 __device__ __forceinline__ void group_sync(int id) {
-  if (id == 1) asm volatile("bar.sync 1, %0;\n" ::"n"(kProducersBar) : "memory");
-  else asm volatile("bar.sync 2, %0;\n" ::"n"(kConsumersBar) : "memory");
+  if (id == 2) asm volatile("bar.sync 2, %0;\n" ::"n"(kConsumersBar) : "memory");
+  else asm volatile("bar.sync %0, %1;\n" ::"r"(id), "n"(kProducersBar) : "memory");
 }
 
-// Shared memory of one row's CTA.  A chunk's K and V rows are staged by
-// cp.async one chunk ahead (two stages); the 16-byte pieces of a K row sit at
-// piece c ^ (key & 7) so that the per-key dot products read without bank
-// conflicts.  The producers then lay the chunk's V out by channel (vt: the
+// Shared memory of one row's CTA.  The chunks of 128 keys alternate between
+// two producer groups; group g stages its chunks' K and V rows into its own
+// stage g by cp.async, one of its chunks ahead; the 16-byte pieces of a K row
+// sit at piece c ^ (key & 7) so that the per-key dot products read without
+// bank conflicts.  The producers then lay the chunk's V out by channel (vt: the
 // offset-binary bytes v + 128 of one channel for the chunk's 128 keys, 16-key
 // piece j at piece j ^ ((channel / 4) mod 8), so that both the transposing
 // stores and the chain threads' 16-byte loads spread over all bank groups).
 constexpr int kChainThreads = kD;                 // one per channel
 constexpr int kSumThreads = 32;                   // the warp that walks the row sum
 constexpr int kConsumers = kChainThreads + kSumThreads;
-constexpr int kProducers = kChunk;                // one per key of a chunk
-constexpr int kExactThreads = kConsumers + kProducers;
+constexpr int kProducers = kChunk;                // one per key of a chunk, per group
+constexpr int kExactThreads = kConsumers + 2 * kProducers;
 constexpr int kSubs = kChunk / kSub;
 
 struct ExactSmem {
-  int8_t k[2][kChunk][kD];
-  uint8_t v[2][kChunk][kD];                       // as the cache holds them
-  uint8_t vt[2][kD][kChunk];                      // by channel, offset binary
+  int8_t k[2][kChunk][kD];                        // [group]
+  uint8_t v[2][kChunk][kD];                       // [group], as the cache holds them
+  uint8_t vt[2][kD][kChunk];                      // [c & 1] by channel, offset binary
   float2 pv[2][kChunk];                           // per key: round_p(p), v_scale
   float2 ap[2][kChunk];                           // per key: alpha, p
   int same[2][kSubs];                             // every alpha of the 32 keys is exactly 1
   ExpfConsts c;
   uint64_t full[2];                               // chunk c's pv, ap, same, vt are ready: full[c & 1]
   uint64_t empty[2];                              // the chains are done with chunk c: empty[c & 1]
-  int row[2][kChunk];                             // plane rows of the stage's keys
+  uint64_t carried[2];                            // carry[c & 3] holds the running max through chunk c
+  int row[2][kChunk];                             // [group] plane rows of the stage's keys
   uint32_t q8[kD / 4];
-  float red[kChunk / 32];
-  float carry;
+  float red[2][kChunk / 32];                      // [group] per-warp maxima
+  float carry[4];                                 // four slots: chunk c's is read at chunk c + 1
+                                                  // and rewritten at chunk c + 4
+  float qs;                                       // the query's int8 scale
   float lsum;                                     // the row sum, for the final division
-  int ok_p, ok_c;                                 // group-wide outcome of a bounded wait
+  int ok_p[2], ok_c;                              // group-wide outcome of a bounded wait
 };
 
-// One CTA of 288 threads per query row, in two groups that overlap chunks:
-//   producers (128 threads, one per key of a chunk): stage chunk c + 1, then
-//     chunk c's scores, prefix max and exps -> pv, ap [c & 1], and chunk c's
-//     V by channel -> vt[c & 1];
+// One CTA of 416 threads per query row, in three groups that overlap chunks:
+//   producers, two groups of 128 threads (one per key of a chunk): group g
+//     takes chunks c = g, g + 2, ...: stages chunk c + 2, then chunk c's
+//     scores and V by channel -> vt[c & 1], its prefix max, and -- once the
+//     running max through chunk c - 1 has come from the other group, and its
+//     own through chunk c has gone back -- its exps -> pv, ap [c & 1];
 //   consumers: the chains (128 threads, one per channel) walk chunk c's o
-//     chain and one warp its l chain, while the producers work on chunk c + 1.
-// A stage is handed over through full / empty mbarriers; one thread of each
-// group waits (bounded) and the group learns the outcome at a group barrier.
+//     chain and one warp its l chain, while the producers work on later chunks.
+// Chunks are handed over through full / empty mbarriers, running maxima
+// through carried; one thread of a group waits (bounded) and the group
+// learns the outcome at a group barrier.
 //
 // Where every alpha of a run of 32 keys is exactly 1 (the running max did not
 // move), the chain steps o = o * alpha + term and l = l * alpha + p are taken
 // as o = o + term and l = l + p: multiplying by 1 is exact, so the bits are
 // the same and each step is one rounding shorter.
-__global__ void __launch_bounds__(kExactThreads)
+__global__ void __launch_bounds__(kExactThreads, 2)
 decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
   extern __shared__ __align__(16) unsigned char exact_smem[];
   ExactSmem& sm = *reinterpret_cast<ExactSmem*>(exact_smem);
@@ -162,8 +169,8 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
     for (int s = 0; s < 2; ++s) {
       ex_mbar_init(&sm.full[s], 1);
       ex_mbar_init(&sm.empty[s], 1);
+      ex_mbar_init(&sm.carried[s], 1);
     }
-    sm.carry = -INFINITY;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -177,10 +184,12 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
 
   if (producer) {
     // ---------------------------------------------------------- producers
-    const int gt = tid - kConsumers;              // key of the chunk
+    const int grp = (tid - kConsumers) / kProducers;   // group: chunks c with c % 2 == grp
+    const int gt = tid - kConsumers - grp * kProducers;   // key of the chunk
     const int lane = gt & 31, gwarp = gt >> 5;
+    const int bar = grp == 0 ? 1 : 3;
     float ks_next = 0.0f, vs_next = 0.0f;
-    auto stage_rows = [&](int t0, int st) {
+    auto stage_rows = [&](int t0) {
       const int t = t0 + gt;
       int row = -1;
       if (t < L) {
@@ -188,122 +197,94 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
         ks_next = ksb[row];
         vs_next = vsb[row];
       }
-      sm.row[st][gt] = row;
+      sm.row[grp][gt] = row;
     };
-    auto issue = [&](int t0, int st) {            // after a group barrier publishes the rows
+    auto issue = [&](int t0) {                    // after a group barrier publishes the rows
       const int n = min(kChunk, L - t0);
 #pragma unroll
       for (int i = 0; i < kD / 16; ++i) {
         const int idx = i * kChunk + gt;
         const int u = idx >> 3, c16 = idx & 7;
         if (u < n) {
-          const int64_t off = (int64_t)sm.row[st][u] * kD + c16 * 16;
-          cp_async16(&sm.k[st][u][(c16 ^ (u & 7)) * 16], kbase + off, 16);
-          cp_async16(&sm.v[st][u][c16 * 16], vbase + off, 16);
+          const int64_t off = (int64_t)sm.row[grp][u] * kD + c16 * 16;
+          cp_async16(&sm.k[grp][u][(c16 ^ (u & 7)) * 16], kbase + off, 16);
+          cp_async16(&sm.v[grp][u][c16 * 16], vbase + off, 16);
         }
       }
       cp_async_commit();
     };
-    stage_rows(0, 0);
-    group_sync(1);
-    issue(0, 0);
+    if (grp < nchunks) {
+      stage_rows(grp * kChunk);
+      group_sync(bar);
+      issue(grp * kChunk);
+    }
 
-    // int8 query: absmax over the 128 channels, then one IEEE division each;
-    // every producer then keeps the whole quantized row in registers.
-    const float x = p.q[qrow * kD + gt];
-    float amax = warp_max(fabsf(x));
-    if (lane == 0) sm.red[gwarp] = amax;
-    group_sync(1);
-    amax = fmaxf(fmaxf(sm.red[0], sm.red[1]), fmaxf(sm.red[2], sm.red[3]));
-    const float qs = quant_scale(amax);
-    reinterpret_cast<int8_t*>(sm.q8)[gt] = (int8_t)quant_one(x, qs);
-    group_sync(1);                                // q8 complete; red free again
-    uint32_t q8[kD / 4];
-#pragma unroll
-    for (int w = 0; w < kD / 4; ++w) q8[w] = sm.q8[w];
+    // int8 query (group 0): absmax over the 128 channels, then one IEEE
+    // division each.  Both groups wait for it at the CTA's barrier 4.
+    if (grp == 0) {
+      const float x = p.q[qrow * kD + gt];
+      float amax = warp_max(fabsf(x));
+      if (lane == 0) sm.red[0][gwarp] = amax;
+      group_sync(bar);
+      amax = fmaxf(fmaxf(sm.red[0][0], sm.red[0][1]), fmaxf(sm.red[0][2], sm.red[0][3]));
+      reinterpret_cast<int8_t*>(sm.q8)[gt] = (int8_t)quant_one(x, quant_scale(amax));
+      if (gt == 0) sm.qs = quant_scale(amax);
+    }
+    asm volatile("bar.sync 4, %0;\n" ::"n"(2 * kProducers) : "memory");
+    const float qs = sm.qs;
 
-    for (int c = 0; c < nchunks; ++c) {
-      const int st = c & 1, tb = st, t0 = c * kChunk, t = t0 + gt;   // K/V stage, buffers
+    for (int c = grp; c < nchunks; c += 2) {
+      const int tb = c & 1, t0 = c * kChunk, t = t0 + gt;
       const bool live = t < L;
       const int n = min(kChunk, L - t0);
       const float ks_cur = ks_next, vs_cur = vs_next;
-      // The consumers must be done with chunk c - 2: its pv, ap and vt
-      // buffers take chunk c.
-      if (c >= 2) {
-        if (gt == 0) {
-          sm.ok_p = ex_mbar_wait(&sm.empty[tb], ((c - 2) >> 1) & 1);
-          if (!sm.ok_p && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
-        }
-        group_sync(1);
-        if (!sm.ok_p) break;                      // the copies in flight drain below
-      }
-      // Stage chunk c + 1 into the K/V stage chunk c - 1 left (read only by
-      // this group, before the barrier that ended the previous chunk).
-      if (c + 1 < nchunks) {
-        stage_rows(t0 + kChunk, st ^ 1);
-        group_sync(1);
-        issue(t0 + kChunk, st ^ 1);
-      } else {
-        cp_async_commit();                        // an empty group keeps the count
-      }
-      cp_async_wait<1>();                         // this chunk's copies (own) landed
-      group_sync(1);                              // ... and the whole group's
+      cp_async_wait<0>();                         // this chunk's copies (own) landed
+      group_sync(bar);                            // ... and the whole group's
 
       float s = -INFINITY;
       if (live) {
         // four partial sums (integers: any order gives the same total)
-        const int4* krow = reinterpret_cast<const int4*>(sm.k[st][gt]);
+        const int4* krow = reinterpret_cast<const int4*>(sm.k[grp][gt]);
+        const uint4* qw = reinterpret_cast<const uint4*>(sm.q8);
         int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
 #pragma unroll
         for (int cc = 0; cc < kD / 16; ++cc) {
           const int4 kv = krow[cc ^ (gt & 7)];
-          a0 = __dp4a((int)kv.x, (int)q8[4 * cc + 0], a0);
-          a1 = __dp4a((int)kv.y, (int)q8[4 * cc + 1], a1);
-          a2 = __dp4a((int)kv.z, (int)q8[4 * cc + 2], a2);
-          a3 = __dp4a((int)kv.w, (int)q8[4 * cc + 3], a3);
+          const uint4 q4 = qw[cc];
+          a0 = __dp4a((int)kv.x, (int)q4.x, a0);
+          a1 = __dp4a((int)kv.y, (int)q4.y, a1);
+          a2 = __dp4a((int)kv.z, (int)q4.z, a2);
+          a3 = __dp4a((int)kv.w, (int)q4.w, a3);
         }
         const int acc = (a0 + a1) + (a2 + a3);
         s = __fmul_rn(__fmul_rn((float)acc, __fmul_rn(qs, ks_cur)), p.sm_scale);
       }
-      // Inclusive prefix max over the chunk, seeded with the running max.
+      // Inclusive prefix max within the chunk (the running max joins below).
       float pm = s;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float o2 = __shfl_up_sync(0xffffffffu, pm, off);
         if (lane >= off) pm = fmaxf(pm, o2);
       }
-      if (lane == 31) sm.red[gwarp] = pm;
-      const float carry = sm.carry;
-      group_sync(1);
-      for (int w = 0; w < gwarp; ++w) pm = fmaxf(pm, sm.red[w]);
-      pm = fmaxf(pm, carry);
-      // Running max before this key: the previous lane's inclusive max, or for
-      // a warp's first lane the max of the carry and all earlier warps.
-      float prev = __shfl_up_sync(0xffffffffu, pm, 1);
-      if (lane == 0) {
-        float pw = carry;
-        for (int w = 0; w < gwarp; ++w) pw = fmaxf(pw, sm.red[w]);
-        prev = pw;
+      if (lane == 31) sm.red[grp][gwarp] = pm;
+      // The consumers must be done with chunk c - 2: its vt, pv, ap buffers
+      // take chunk c.
+      if (c >= 2 && gt == 0) {
+        sm.ok_p[grp] = ex_mbar_wait(&sm.empty[tb], ((c - 2) >> 1) & 1);
+        if (!sm.ok_p[grp] && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
       }
-      float a = 1.0f;
-      if (live) {
-        // expf_tang(0) is exactly 1: skip the double-precision steps when the
-        // running max did not move.
-        a = prev == pm ? 1.0f : expf_tang(__fsub_rn(prev, pm), sm.c);
-        const float pp = s == pm ? 1.0f : expf_tang(__fsub_rn(s, pm), sm.c);
-        sm.pv[tb][gt] = make_float2(round_p_exact(pp, p.p_mode), vs_cur);
-        sm.ap[tb][gt] = make_float2(a, pp);
-      }
-      // warp gwarp holds keys 32 gwarp .. + 31: its run of alphas
-      const bool same = __all_sync(0xffffffffu, a == 1.0f);
-      if (lane == 0) sm.same[tb][gwarp] = same ? 1 : 0;
+      group_sync(bar);
+      if (c >= 2 && !sm.ok_p[grp]) break;         // the copies in flight drain below
+      float pw = -INFINITY;                       // maximum of the earlier warps of the chunk
+      for (int w = 0; w < gwarp; ++w) pw = fmaxf(pw, sm.red[grp][w]);
+      pm = fmaxf(pm, pw);
       // Chunk c's V by channel: thread (kb = gwarp, g4 = lane) transposes keys
       // 32 kb .. + 31 of channels 4 g4 .. + 3, in 4 x 4 byte blocks.
       {
         uint32_t w[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k)
-          w[k] = *reinterpret_cast<const uint32_t*>(&sm.v[st][32 * gwarp + k][4 * lane]);
+          w[k] = *reinterpret_cast<const uint32_t*>(&sm.v[grp][32 * gwarp + k][4 * lane]);
         uint32_t ot[4][8];                        // [channel i][keys 4q .. 4q + 3]
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -326,8 +307,47 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
                 make_uint4(ot[i][4 * hh], ot[i][4 * hh + 1], ot[i][4 * hh + 2], ot[i][4 * hh + 3]);
           }
       }
-      group_sync(1);                              // chunk c published; red and carry reads done
-      if (gt == n - 1) sm.carry = pm;
+      group_sync(bar);                            // stage grp read (K and V); red reads done
+      // Stage this group's next chunk, c + 2, into its stage.
+      if (c + 2 < nchunks) {
+        stage_rows(t0 + 2 * kChunk);
+        group_sync(bar);
+        issue(t0 + 2 * kChunk);
+      }
+      // The running max through chunk c - 1, from the other group.
+      float carry = -INFINITY;
+      if (c >= 1) {
+        if (gt == 0) {
+          sm.ok_p[grp] = ex_mbar_wait(&sm.carried[(c - 1) & 1], ((c - 1) >> 1) & 1);
+          if (!sm.ok_p[grp] && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
+        }
+        group_sync(bar);
+        if (!sm.ok_p[grp]) break;
+        carry = sm.carry[(c - 1) & 3];
+      }
+      // Running max before this key: the previous lane's inclusive max, or for
+      // a warp's first lane the max of the carry and all earlier warps.
+      float prev = __shfl_up_sync(0xffffffffu, pm, 1);
+      if (lane == 0) prev = pw;
+      prev = fmaxf(prev, carry);
+      pm = fmaxf(pm, carry);
+      if (gt == n - 1) {                          // the running max through chunk c
+        sm.carry[c & 3] = pm;
+        ex_mbar_arrive(&sm.carried[tb]);
+      }
+      float a = 1.0f;
+      if (live) {
+        // expf_tang(0) is exactly 1: skip the double-precision steps when the
+        // running max did not move.
+        a = prev == pm ? 1.0f : expf_tang(__fsub_rn(prev, pm), sm.c);
+        const float pp = s == pm ? 1.0f : expf_tang(__fsub_rn(s, pm), sm.c);
+        sm.pv[tb][gt] = make_float2(round_p_exact(pp, p.p_mode), vs_cur);
+        sm.ap[tb][gt] = make_float2(a, pp);
+      }
+      // warp gwarp holds keys 32 gwarp .. + 31: its run of alphas
+      const bool same = __all_sync(0xffffffffu, a == 1.0f);
+      if (lane == 0) sm.same[tb][gwarp] = same ? 1 : 0;
+      group_sync(bar);                            // chunk c published
       if (gt == 0) ex_mbar_arrive(&sm.full[tb]);
     }
     cp_async_wait<0>();
