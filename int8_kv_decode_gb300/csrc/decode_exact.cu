@@ -121,15 +121,16 @@ struct ExactSmem {
                                                   // and rewritten at chunk c + 4
   float qs;                                       // the query's int8 scale
   float lsum;                                     // the row sum, for the final division
-  int ok_p[2], ok_c;                              // group-wide outcome of a bounded wait
+  int ok_carry[2], ok_empty[2], ok_c;             // group-wide outcomes of bounded waits
 };
 
 // One CTA of 416 threads per query row, in three groups that overlap chunks:
 //   producers, two groups of 128 threads (one per key of a chunk): group g
-//     takes chunks c = g, g + 2, ...: stages chunk c + 2, then chunk c's
-//     scores and V by channel -> vt[c & 1], its prefix max, and -- once the
-//     running max through chunk c - 1 has come from the other group, and its
-//     own through chunk c has gone back -- its exps -> pv, ap [c & 1];
+//     takes chunks c = g, g + 2, ...: chunk c's scores and prefix max; once the
+//     running max through chunk c - 1 has come from the other group (and its
+//     own through chunk c has gone back), its exps; once the consumers are
+//     done with chunk c - 2, its pv, ap and V by channel -> [c & 1]; then it
+//     stages chunk c + 2;
 //   consumers: the chains (128 threads, one per channel) walk chunk c's o
 //     chain and one warp its l chain, while the producers work on later chunks.
 // Chunks are handed over through full / empty mbarriers, running maxima
@@ -267,17 +268,49 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
         if (lane >= off) pm = fmaxf(pm, o2);
       }
       if (lane == 31) sm.red[grp][gwarp] = pm;
-      // The consumers must be done with chunk c - 2: its vt, pv, ap buffers
-      // take chunk c.
-      if (c >= 2 && gt == 0) {
-        sm.ok_p[grp] = ex_mbar_wait(&sm.empty[tb], ((c - 2) >> 1) & 1);
-        if (!sm.ok_p[grp] && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
+      // The running max through chunk c - 1, from the other group.
+      if (c >= 1 && gt == 0) {
+        sm.ok_carry[grp] = ex_mbar_wait(&sm.carried[(c - 1) & 1], ((c - 1) >> 1) & 1);
+        if (!sm.ok_carry[grp] && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
       }
-      group_sync(bar);
-      if (c >= 2 && !sm.ok_p[grp]) break;         // the copies in flight drain below
+      group_sync(bar);                            // red written; the carry's outcome
+      if (c >= 1 && !sm.ok_carry[grp]) break;     // the copies in flight drain below
+      const float carry = c >= 1 ? sm.carry[(c - 1) & 3] : -INFINITY;
       float pw = -INFINITY;                       // maximum of the earlier warps of the chunk
       for (int w = 0; w < gwarp; ++w) pw = fmaxf(pw, sm.red[grp][w]);
       pm = fmaxf(pm, pw);
+      // Running max before this key: the previous lane's inclusive max, or for
+      // a warp's first lane the max of the carry and all earlier warps.
+      float prev = __shfl_up_sync(0xffffffffu, pm, 1);
+      if (lane == 0) prev = pw;
+      prev = fmaxf(prev, carry);
+      pm = fmaxf(pm, carry);
+      if (gt == n - 1) {                          // the running max through chunk c
+        sm.carry[c & 3] = pm;
+        ex_mbar_arrive(&sm.carried[tb]);
+      }
+      // expf_tang(0) is exactly 1: skip the double-precision steps when the
+      // running max did not move.
+      float a = 1.0f, pp = 0.0f;
+      if (live) {
+        a = prev == pm ? 1.0f : expf_tang(__fsub_rn(prev, pm), sm.c);
+        pp = s == pm ? 1.0f : expf_tang(__fsub_rn(s, pm), sm.c);
+      }
+      // warp gwarp holds keys 32 gwarp .. + 31: its run of alphas
+      const bool same = __all_sync(0xffffffffu, a == 1.0f);
+      // The consumers must be done with chunk c - 2: its vt, pv, ap buffers
+      // take chunk c.
+      if (c >= 2 && gt == 0) {
+        sm.ok_empty[grp] = ex_mbar_wait(&sm.empty[tb], ((c - 2) >> 1) & 1);
+        if (!sm.ok_empty[grp] && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
+      }
+      group_sync(bar);                            // red reads done; the release's outcome
+      if (c >= 2 && !sm.ok_empty[grp]) break;
+      if (live) {
+        sm.pv[tb][gt] = make_float2(round_p_exact(pp, p.p_mode), vs_cur);
+        sm.ap[tb][gt] = make_float2(a, pp);
+      }
+      if (lane == 0) sm.same[tb][gwarp] = same ? 1 : 0;
       // Chunk c's V by channel: thread (kb = gwarp, g4 = lane) transposes keys
       // 32 kb .. + 31 of channels 4 g4 .. + 3, in 4 x 4 byte blocks.
       {
@@ -307,48 +340,14 @@ decode_exact_kernel(DecodeParams p, ExpfConsts consts) {
                 make_uint4(ot[i][4 * hh], ot[i][4 * hh + 1], ot[i][4 * hh + 2], ot[i][4 * hh + 3]);
           }
       }
-      group_sync(bar);                            // stage grp read (K and V); red reads done
+      group_sync(bar);                            // chunk c published; stage grp read
+      if (gt == 0) ex_mbar_arrive(&sm.full[tb]);
       // Stage this group's next chunk, c + 2, into its stage.
       if (c + 2 < nchunks) {
         stage_rows(t0 + 2 * kChunk);
         group_sync(bar);
         issue(t0 + 2 * kChunk);
       }
-      // The running max through chunk c - 1, from the other group.
-      float carry = -INFINITY;
-      if (c >= 1) {
-        if (gt == 0) {
-          sm.ok_p[grp] = ex_mbar_wait(&sm.carried[(c - 1) & 1], ((c - 1) >> 1) & 1);
-          if (!sm.ok_p[grp] && p.err_word != nullptr) atomicOr(p.err_word, KATTN_DEVERR_TIMEOUT);
-        }
-        group_sync(bar);
-        if (!sm.ok_p[grp]) break;
-        carry = sm.carry[(c - 1) & 3];
-      }
-      // Running max before this key: the previous lane's inclusive max, or for
-      // a warp's first lane the max of the carry and all earlier warps.
-      float prev = __shfl_up_sync(0xffffffffu, pm, 1);
-      if (lane == 0) prev = pw;
-      prev = fmaxf(prev, carry);
-      pm = fmaxf(pm, carry);
-      if (gt == n - 1) {                          // the running max through chunk c
-        sm.carry[c & 3] = pm;
-        ex_mbar_arrive(&sm.carried[tb]);
-      }
-      float a = 1.0f;
-      if (live) {
-        // expf_tang(0) is exactly 1: skip the double-precision steps when the
-        // running max did not move.
-        a = prev == pm ? 1.0f : expf_tang(__fsub_rn(prev, pm), sm.c);
-        const float pp = s == pm ? 1.0f : expf_tang(__fsub_rn(s, pm), sm.c);
-        sm.pv[tb][gt] = make_float2(round_p_exact(pp, p.p_mode), vs_cur);
-        sm.ap[tb][gt] = make_float2(a, pp);
-      }
-      // warp gwarp holds keys 32 gwarp .. + 31: its run of alphas
-      const bool same = __all_sync(0xffffffffu, a == 1.0f);
-      if (lane == 0) sm.same[tb][gwarp] = same ? 1 : 0;
-      group_sync(bar);                            // chunk c published
-      if (gt == 0) ex_mbar_arrive(&sm.full[tb]);
     }
     cp_async_wait<0>();
     return;
