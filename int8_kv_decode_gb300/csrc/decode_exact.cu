@@ -10,9 +10,10 @@
 //
 // Only the l and o chains are inherently serial.  The scores, the running
 // max (a prefix max, which is exact in any order) and every exp are computed
-// in parallel per chunk of 128 keys by one group of threads, while a second
-// group walks the previous chunk's chains (thread i: channel i), reading the
-// chunk's V rows from shared memory.
+// in parallel per chunk of 128 keys, by two producer groups on alternate
+// chunks, while the consumers walk the earlier chunks' chains (thread i:
+// channel i; one warp the row sum), reading each chunk's V laid out by
+// channel in shared memory.
 #include "device_common.cuh"
 
 namespace kattn {
@@ -113,7 +114,8 @@ struct ExactSmem {
   ExpfConsts c;
   uint64_t full[2];                               // chunk c's pv, ap, same, vt are ready: full[c & 1]
   uint64_t empty[2];                              // the chains are done with chunk c: empty[c & 1]
-  uint64_t carried[2];                            // carry[c & 3] holds the running max through chunk c
+  uint64_t carried[2];                            // carried[c & 1]: carry[c & 3] holds the running
+                                                  // max through chunk c
   int row[2][kChunk];                             // [group] plane rows of the stage's keys
   uint32_t q8[kD / 4];
   float red[2][kChunk / 32];                      // [group] per-warp maxima
