@@ -82,7 +82,7 @@ enum kattn_p_mode {
 #define KATTN_DEVERR_BAD_SEQUENCE 0x1u /* row_start / ctx_len out of range */
 #define KATTN_DEVERR_TIMEOUT 0x2u      /* a bounded wait inside a kernel ran out
                                           (a K/V copy, or exact mode's hand-off
-                                          between its two thread groups); the
+                                          between its thread groups); the
                                           affected outputs are not written (fast
                                           mode) or are NaN (exact mode) */
 #define KATTN_DEVERR_BAD_PAGE 0x4u     /* kattn_decode_paged: a block-table entry
@@ -187,8 +187,8 @@ int kattn_quantize_kv_rows(const float* x, int n_rows, int n_kv, int d,
  *   oracle's sequential emulation.  workspace may be NULL; if given (at
  *   least 256 bytes, 256-byte aligned, zeroed before its first use) only its
  *   error word is used: KATTN_DEVERR_BAD_SEQUENCE, and KATTN_DEVERR_TIMEOUT
- *   when a bounded hand-off wait between the kernel's two thread groups ran
- *   out (that row's output is then NaN).
+ *   when a bounded hand-off wait between the kernel's thread groups ran out
+ *   (that row's output is then NaN).
  * out:       float32 [B][M][Hq][d]. */
 int kattn_decode(const float* q, const int8_t* k, const float* k_scale,
                  const int8_t* v, const float* v_scale, const int64_t* row_start,

@@ -1,9 +1,10 @@
 """Exact mode's bounded waits, made to run out on purpose.
 
-The exact-mode kernel runs two thread groups per query row that hand chunks
-of keys to each other through shared-memory barriers; every wait for a
-hand-off is bounded, and one that runs out leaves the row NaN and sets
-KATTN_DEVERR_TIMEOUT in the workspace's error word.  To exercise that path
+The exact-mode kernel runs three thread groups per query row (two producer
+groups and the consumers) that hand chunks of keys and running maxima to each
+other through shared-memory barriers; every wait for a hand-off is bounded,
+and one that runs out leaves the row NaN and sets KATTN_DEVERR_TIMEOUT in the
+workspace's error word.  To exercise that path
 without any wait that could block, this test loads a separate build of the
 library (build.py, build_exact_timeout_variant) in which the waits give up
 after 0 polls: every wait runs out at once, deterministically.  The test
