@@ -127,3 +127,20 @@ def test_kernel_hash_ignores_comments_but_not_code():
     assert bench._code_only(src) == bench._code_only(same)
     assert bench._code_only(src) != bench._code_only(other)
     assert len(bench.kernel_source_sha("decode_fast_kernel")) == 16
+
+
+def test_committed_traffic_lines_match_the_kernel_sources():
+    # Every workload with a traffic line in the committed ncu summary resolves
+    # against the current sources of the kernel that runs it (the summary was
+    # taken from these kernels), and its bytes are close to the algorithmic
+    # bytes of a launch: no K/V byte read twice.
+    import bench
+    cases = [("serving_b256_m1", "decode_fast_kernel", False, 2323.93e6),
+             ("long_128k", "decode_fast_kernel", False, 553.78e6),
+             ("serving_b256_m4", "decode_tc_kernel", False, 2349.91e6),
+             ("spec_verify", "decode_fast_kernel", False, 44.33e6),
+             ("serving_b256_m1_paged64", "decode_fast_kernel", True, 2323.93e6)]
+    for workload, kernel, paged, algorithmic in cases:
+        got = bench.profiled_traffic(workload, bench.kernel_source_sha(kernel, paged=paged))
+        assert got is not None, workload
+        assert 0.9 * algorithmic <= got <= 1.15 * algorithmic, (workload, got)
